@@ -1,0 +1,441 @@
+#!/usr/bin/env python3
+"""Benchmark of the GEMM hot path on GB300.
+
+Metric: GEMM TFLOP/s at M = N = K = 8192, BF16 inputs U[-1,1], FP32
+accumulation, BF16 output, device-timed with CUDA events, and its fraction of
+the dense BF16 tensor peak.  One step = one gemm_bf16 call through the C ABI
+on that workload (host validation, planning, descriptors, the persistent
+2-CTA kernel).  The inputs (256 MiB of A and B) are larger than the 129 MB L2,
+so no flush is needed between timed iterations.
+
+Prints ONE JSON line (rank 0).  Flags: --gpus N --steps K --warmup W
+[--impl reference] [--no-variants].  Under torchrun every rank runs its own
+replica of the workload (the product has no exchange step at one GPU per
+problem) and the slowest rank's time sets the aggregate.
+
+--impl reference times the CPU oracle (FP64 triple loop, test infrastructure)
+on a bounded sample of rows of the same product, on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "GEMM TFLOPS at 8192^3 BF16 (device-timed) and % of dense BF16 tensor peak"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_gemm_8192.txt")
+KERNEL_SOURCES = ["gemm_tc.cu", "ptx.cuh", "layout.h", "params.h", "api.cu"]
+
+
+# ----------------------------------------------------------------- infra ----
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist_mod):
+    if dist_mod is not None:
+        dist_mod.barrier()
+
+
+def max_over_ranks(value: float, dist_mod, device) -> float:
+    """The largest value any rank holds (slowest rank's time)."""
+    if dist_mod is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sms, maxes, power, reasons = [], [], [], set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) != len(self.FIELDS):
+                    continue
+                try:
+                    sms.append(float(parts[0]))
+                    maxes.append(float(parts[1]))
+                    power.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(self.REASONS, parts[4:]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sms) if sms else None,
+                "sm_max_mhz": max(maxes) if maxes else None,
+                "reasons": sorted(reasons), "samples": len(sms),
+                "power_w_max": max(power) if power else None}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "blackwell_tensor_core_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------- timing -------
+
+def time_launches(launch, steps, stream, dist_mod, between=None):
+    """Times `steps` launches on `stream`.  Returns (total_ms, per-launch ms list)."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist_mod)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(steps):
+        if between is not None:
+            between()
+        starts[i].record(stream)
+        launch()
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist_mod)
+    return t0.elapsed_time(t1), [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def dense_launcher(ops, A, B, D, out_code, stream):
+    M, K = A.shape
+    N = B.shape[1]
+    a, b, d, h = A.data_ptr(), B.data_ptr(), D.data_ptr(), stream.cuda_stream
+    return lambda: ops.gemm_bf16(a, b, d, M, N, K, K, N, N, out_code, h)
+
+
+def check_device_error(ops):
+    st, word = ops.last_device_error()
+    if st != 0:
+        raise RuntimeError("device error word %#x (status %d)" % (word, st))
+
+
+# ---------------------------------------------------------------- arms ------
+
+def oracle_rows_tflops(A_bits, B_bits, rows, start_row=0):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.gemm(A_bits, B_bits, rows=(start_row, start_row + rows))
+    dt = time.perf_counter() - t0
+    K = A_bits.shape[1]
+    N = B_bits.shape[1]
+    return 2.0 * rows * N * K / dt / 1e12, dt
+
+
+def cpu_baseline(case, budget_s=12.0):
+    """The oracle as it stands on a bounded row sample of the same product."""
+    import oracle
+    from blackwell_tensor_core_gb300 import workloads as wl
+    oracle.build()
+    Ab, Bb = wl.bits(case.A), wl.bits(case.B)
+    probe = 4
+    _, dt = oracle_rows_tflops(Ab, Bb, probe)
+    rows = int(max(probe, min(case.M, budget_s / max(dt / probe, 1e-9))))
+    val, dt = oracle_rows_tflops(Ab, Bb, rows, probe)
+    return {"value": val, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d rows of the %dx%dx%d product (%d outputs, K=%d), FP64, %.1f s"
+                      % (rows, case.M, case.N, case.K, rows * case.N, case.K, dt)}
+
+
+def run_reference(args, rank):
+    """Reference arm: the CPU oracle on a bounded sample per step (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    from blackwell_tensor_core_gb300 import workloads as wl
+    oracle.build()
+    case = wl.large_case()
+    Ab, Bb = wl.bits(case.A), wl.bits(case.B)
+    _, dt = oracle_rows_tflops(Ab, Bb, 2)
+    per_row = dt / 2
+    rows = max(1, int(120.0 / max((args.steps + args.warmup) * per_row, 1e-9)))
+    rows = min(rows, case.M)
+    for i in range(args.warmup):
+        oracle_rows_tflops(Ab, Bb, rows, (i * rows) % (case.M - rows + 1))
+    vals, times = [], []
+    for i in range(args.steps):
+        v, dt = oracle_rows_tflops(Ab, Bb, rows, ((args.warmup + i) * rows) % (case.M - rows + 1))
+        vals.append(v)
+        times.append(dt)
+    value = 2.0 * rows * case.N * case.K * len(times) / sum(times) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "gemm_8192x8192x8192 (oracle, %d-row sample per step)" % rows,
+                   "M": case.M, "N": case.N, "K": case.K},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": "%d rows of the 8192^3 product per step, FP64 triple loop" % rows},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def measure_variants(ops, wl, stream, dist_mod, peaks, steps):
+    """Shorter measurements of the other method workloads (same JSON line)."""
+    import torch
+    out = {}
+    dev = torch.device("cuda")
+    # small-M swapped kernel: HBM-bound, report algorithmic GB/s
+    c = wl.small_m_case()
+    A, B = c.A.to(dev), c.B.to(dev)
+    D = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=dev)
+    launch = dense_launcher(ops, A, B, D, wl.OUT_BF16, stream)
+    for _ in range(5):
+        launch()
+    _, per = time_launches(launch, steps, stream, dist_mod)
+    check_device_error(ops)
+    ms = statistics.mean(per)
+    nbytes = 2 * (c.M * c.K + c.K * c.N + c.M * c.N)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["small_m_72x16384x7168"] = {
+        "ms_per_launch": ms, "tflops": c.flops / (ms * 1e-3) / 1e12,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": nbytes},
+        "l2": "B (235 MB) larger than L2"}
+    del A, B, D
+    # square 4096: inputs fit in L2, so flush L2 between timed launches
+    c = wl.square_case()
+    A, B = c.A.to(dev), c.B.to(dev)
+    D = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    launch = dense_launcher(ops, A, B, D, wl.OUT_BF16, stream)
+    for _ in range(5):
+        launch()
+    _, per = time_launches(launch, steps, stream, dist_mod, between=lambda: flush.zero_())
+    check_device_error(ops)
+    ms = statistics.mean(per)
+    tf = c.flops / (ms * 1e-3) / 1e12
+    out["square_4096"] = {"ms_per_launch": ms, "tflops": tf,
+                          "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                                       "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"]},
+                          "l2": "flushed (256 MiB write) before every timed launch"}
+    del A, B, D, flush
+    # grouped expert FC1
+    c = wl.grouped_case()
+    A = c.A.to(dev)
+    Bs = [b.to(dev) for b in c.Bs]
+    off = torch.from_numpy(c.offsets).to(dev)
+    D = torch.empty((c.total, c.N), dtype=torch.bfloat16, device=dev)
+    bptrs = [b.data_ptr() for b in Bs]
+    a, d, o, h = A.data_ptr(), D.data_ptr(), off.data_ptr(), stream.cuda_stream
+
+    def glaunch():
+        ops.grouped_gemm_bf16(a, bptrs, d, o, c.G, c.total, c.N, c.K, h)
+    for _ in range(3):
+        glaunch()
+    _, per = time_launches(glaunch, max(5, steps // 4), stream, dist_mod)
+    check_device_error(ops)
+    ms = statistics.mean(per)
+    tf = c.flops / (ms * 1e-3) / 1e12
+    out["grouped_fc1_32x4096x4096"] = {
+        "ms_per_launch": ms, "tflops": tf, "rows": c.total,
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tf / peaks["bf16_tflops"]},
+        "l2": "A + B (1.34 GB) larger than L2"}
+    return out
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from blackwell_tensor_core_gb300 import build, ops
+    from blackwell_tensor_core_gb300 import workloads as wl
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device (there is no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_mod = init_dist(world, "nccl")
+    build.build()
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    case = wl.large_case()
+    A, B = case.A.to(dev), case.B.to(dev)
+    D = torch.empty((case.M, case.N), dtype=torch.bfloat16, device=dev)
+    launch = dense_launcher(ops, A, B, D, wl.OUT_BF16, stream)
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    check_device_error(ops)
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    total_ms, per = time_launches(launch, args.steps, stream, dist_mod)
+    clocks = sampler.stop()
+    check_device_error(ops)
+    total_ms = max_over_ranks(total_ms, dist_mod, dev)
+
+    flops = case.flops
+    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    mean_launch = statistics.mean(per)
+    achieved = flops / (mean_launch * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    traffic = recorded_traffic()
+    plan = ops.plan(case.M, case.N, case.K, sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
+
+    # end to end through the host-buffer entry point (copies in the timed region)
+    hA, hB = case.A.pin_memory(), case.B.pin_memory()
+    hD = torch.empty((case.M, case.N), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def e2e_launch():
+        ops.gemm_bf16_host(hA, hB, hD, A, B, D, stream)
+    e2e_launch()
+    torch.cuda.synchronize()
+    e2e_ms, _ = time_launches(e2e_launch, e2e_steps, stream, dist_mod)
+    e2e_ms = max_over_ranks(e2e_ms, dist_mod, dev)
+    check_device_error(ops)
+    e2e = {"value": flops * e2e_steps * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": 2 * case.M * case.K + 2 * case.K * case.N,
+           "d2h_bytes_per_step": 2 * case.M * case.N, "steps": e2e_steps,
+           "api": "gemm_bf16_host (pinned host buffers, H2D + GEMM + D2H on one stream)"}
+    del hA, hB, hD
+
+    variants = None
+    if not args.no_variants:
+        variants = measure_variants(ops, wl, stream, dist_mod, peaks, min(args.steps, 100))
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "gemm_8192x8192x8192_bf16in_fp32acc_bf16out", "M": case.M, "N": case.N,
+                   "K": case.K, "inputs": "U[-1,1], seed 1003, row-major A and B",
+                   "l2": "inputs larger than L2 (A+B = 256 MiB > 129 MB); no flush",
+                   "kernel": "persistent 2-CTA 256x256x64, %d stages, grid %d" % (plan.stages, plan.grid),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": "%s bf16_tflops_sustained (kernel timed inside a back-to-back loop)" % peak_src,
+                     "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
+                     "algorithmic_flops_per_launch": flops,
+                     "algorithmic_bytes_per_launch": 3 * 2 * case.M * case.N},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "launch_ms": {"mean": mean_launch, "median": statistics.median(per), "min": min(per), "max": max(per)},
+        "variants": variants,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,579 @@
+// Host runtime and C ABI: argument checks, the planner (kernel, tile, ring
+// depth and grid choice), the TMA descriptor cache and the launches.
+//
+// Planner rules ("B200 的 2CTA 怎样调优", sections 三 and 八): large problems
+// take 256x256 tiles on CTA pairs, with the deepest SMEM ring that fits after
+// the epilogue's staging buffers; a problem whose M is at most 128 rows would
+// waste half or more of a 256-row tile, so it takes the swapped narrow-N
+// kernel instead ("MegaMoE …", section 04).  The persistent grid is the number
+// of co-resident clusters the occupancy API reports, capped by the tile count.
+// Tensor descriptors ("GEMM优化（三）", section 4.2): 2-D tiled maps with
+// 128-byte swizzle and 256-byte L2 promotion; out-of-range boxes fill zeros.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/bwgemm.h"
+#include "layout.h"
+#include "params.h"
+
+namespace bwg {
+cudaError_t set_gemm_attributes(size_t smem);
+cudaError_t set_small_m_attributes(size_t smem);
+}  // namespace bwg
+
+using namespace bwg;
+
+namespace {
+
+// Device error word: one per device per process, written by kernels that
+// give up on a barrier wait (see bwg_last_device_error).
+__device__ unsigned long long g_device_error_word;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+std::atomic<unsigned> g_tx_extra{0};
+
+constexpr int kMaxDevices = 64;
+constexpr int kBarrierArea = 2048;  // barriers, TMEM address slot, grouped tables
+constexpr int kGroupM = 8;
+
+struct DeviceState {
+  bool ready = false;
+  bwg_status init_status = BWG_OK;
+  int sm_count = 0;
+  int max_smem = 0;
+  unsigned long long* err = nullptr;
+  int clusters_2cta = 0;
+  int ctas_1cta = 0;
+  int clusters_grouped = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+struct MapKey {
+  const void* ptr;
+  uint64_t inner, outer, row_bytes;
+  uint32_t box_inner, box_outer;
+  int dtype, swizzle, device;
+  bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    const uint64_t* w = reinterpret_cast<const uint64_t*>(&k);
+    uint64_t h = 1469598103934665603ull;
+    for (size_t i = 0; i < sizeof(MapKey) / 8; ++i) h = (h ^ w[i]) * 1099511628211ull;
+    return static_cast<size_t>(h);
+  }
+};
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+// ------------------------------------------------------------ planning -----
+
+int dense_stage_bytes(int cg) { return kRowsPerCta * kBK * 2 + (kTileN / cg) * kBK * 2; }
+
+int dense_smem(int cg, int stages) { return 1024 + stages * dense_stage_bytes(cg) + kEpiBytes + kBarrierArea; }
+
+int small_m_pad(int M) { return std::max(16, (M + 15) & ~15); }
+
+int small_m_stage_bytes(int m_pad) { return 128 * kBK * 2 + m_pad * kBK * 2; }
+
+int small_m_staging(int m_pad, int out_dtype) { return 2 * m_pad * 64 * (out_dtype == kOutF32 ? 4 : 2); }
+
+int small_m_smem(int m_pad, int out_dtype, int stages) {
+  return 1024 + stages * small_m_stage_bytes(m_pad) + 1024 + small_m_staging(m_pad, out_dtype) + 512;
+}
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_count, int max_smem,
+                      int force_kernel, int force_stages, int max_clusters_2cta, int max_ctas_1cta,
+                      bwg_plan_info* o) {
+  std::memset(o, 0, sizeof(*o));
+  if (M == 0 || N == 0) {
+    o->kernel = BWG_KERNEL_NONE;
+    return BWG_OK;
+  }
+  if (K == 0) {
+    o->kernel = BWG_KERNEL_ZERO;
+    return BWG_OK;
+  }
+  int kind = force_kernel;
+  if (kind == 0) kind = (M <= kSmallMMaxM) ? BWG_KERNEL_SMALL_M : BWG_KERNEL_2CTA;
+  if (kind != BWG_KERNEL_1CTA && kind != BWG_KERNEL_2CTA && kind != BWG_KERNEL_SMALL_M)
+    return BWG_ERR_INVALID_ARG;
+  if (kind == BWG_KERNEL_SMALL_M && M > kSmallMMaxM) return BWG_ERR_UNSUPPORTED;
+  const uint32_t fmt = fp16_in ? kFmtF16 : kFmtBF16;
+  o->kernel = kind;
+  o->tile_k = kBK;
+  o->k_blocks = ceil_div(K, kBK);
+  if (kind == BWG_KERNEL_SMALL_M) {
+    const int m_pad = small_m_pad(M);
+    o->tile_m = m_pad;
+    o->tile_n = 128;
+    o->mma_m = 128;
+    o->mma_n = m_pad;
+    const int fixed = small_m_smem(m_pad, out_dtype, 0);
+    int stages = std::min(8, (max_smem - fixed) / small_m_stage_bytes(m_pad));
+    if (force_stages > 0) stages = force_stages;
+    if (stages < 2 || small_m_smem(m_pad, out_dtype, stages) > max_smem) return BWG_ERR_UNSUPPORTED;
+    o->stages = stages;
+    o->tiles = ceil_div(N, 128);
+    o->smem_input_per_cta = stages * small_m_stage_bytes(m_pad);
+    o->smem_total = small_m_smem(m_pad, out_dtype, stages);
+    o->grid = std::min(o->tiles, sm_count);
+    o->tx_bytes = static_cast<uint32_t>(small_m_stage_bytes(m_pad));
+    o->idesc = make_idesc_f16(fmt, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, m_pad);
+  } else {
+    const int cg = (kind == BWG_KERNEL_2CTA) ? 2 : 1;
+    o->tile_m = kRowsPerCta * cg;
+    o->tile_n = kTileN;
+    o->mma_m = kRowsPerCta * cg;
+    o->mma_n = kTileN;
+    const int fixed = dense_smem(cg, 0);
+    int stages = std::min(8, (max_smem - fixed) / dense_stage_bytes(cg));
+    if (force_stages > 0) stages = force_stages;
+    if (stages < 2 || dense_smem(cg, stages) > max_smem) return BWG_ERR_UNSUPPORTED;
+    o->stages = stages;
+    o->tiles = ceil_div(M, o->tile_m) * ceil_div(N, o->tile_n);
+    o->smem_input_per_cta = stages * dense_stage_bytes(cg);
+    o->smem_total = dense_smem(cg, stages);
+    if (cg == 2)
+      o->grid = 2 * std::min(o->tiles, max_clusters_2cta > 0 ? max_clusters_2cta : sm_count / 2);
+    else
+      o->grid = std::min(o->tiles, max_ctas_1cta > 0 ? max_ctas_1cta : sm_count);
+    o->tx_bytes = static_cast<uint32_t>(cg * dense_stage_bytes(cg));
+    o->idesc = make_idesc_f16(fmt, /*a_mn_major=*/false, /*b_mn_major=*/true, o->mma_m, kTileN);
+  }
+  o->coverage = static_cast<double>(M) * N / (static_cast<double>(o->tiles) * o->tile_m * o->tile_n);
+  return BWG_OK;
+}
+
+int out_elt(int out_dtype) { return out_dtype == BWG_OUT_FP32 ? 4 : 2; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bwg_status check_args(const void* A, const void* B, const void* D, int M, int N, int K, int lda,
+                      int ldb, int ldd, int out_dtype) {
+  if (out_dtype != BWG_OUT_BF16 && out_dtype != BWG_OUT_FP32 && out_dtype != BWG_OUT_FP16)
+    return BWG_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return BWG_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return BWG_OK;
+  if (D == nullptr || ldd < N) return BWG_ERR_INVALID_ARG;
+  if (K > 0 && (A == nullptr || B == nullptr || lda < K || ldb < N)) return BWG_ERR_INVALID_ARG;
+  if (!aligned16(D) || (static_cast<long long>(ldd) * out_elt(out_dtype)) % 16 != 0)
+    return BWG_ERR_ALIGNMENT;
+  if (K > 0 && (!aligned16(A) || !aligned16(B) || (static_cast<long long>(lda) * 2) % 16 != 0 ||
+                (static_cast<long long>(ldb) * 2) % 16 != 0))
+    return BWG_ERR_ALIGNMENT;
+  return BWG_OK;
+}
+
+// ------------------------------------------------------------- devices -----
+
+bwg_status ensure_device(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return BWG_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return BWG_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    st.ready = true;
+    st.init_status = BWG_OK;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      st.init_status = BWG_ERR_CUDA;
+    } else if (major != 10 || minor != 3) {
+      st.init_status = BWG_ERR_UNSUPPORTED;  // the library carries sm_103a code only
+    }
+    if (st.init_status == BWG_OK && g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        cudaGetLastError();
+        st.init_status = BWG_ERR_CUDA;
+      } else {
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+      }
+    }
+    if (st.init_status == BWG_OK) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess ||
+          cudaMemset(p, 0, sizeof(unsigned long long)) != cudaSuccess) {
+        cudaGetLastError();
+        st.init_status = BWG_ERR_CUDA;
+      } else {
+        st.err = static_cast<unsigned long long*>(p);
+      }
+    }
+    if (st.init_status == BWG_OK) {
+      if (set_gemm_attributes(st.max_smem) != cudaSuccess ||
+          set_small_m_attributes(st.max_smem) != cudaSuccess) {
+        cudaGetLastError();
+        st.init_status = BWG_ERR_CUDA;
+      } else {
+        st.clusters_2cta = max_active_clusters_gemm(2, false, dense_smem(2, 6));
+        st.clusters_grouped = max_active_clusters_gemm(2, true, dense_smem(2, 6));
+        st.ctas_1cta = max_active_clusters_gemm(1, false, dense_smem(1, 4));
+        if (st.clusters_2cta <= 0) st.clusters_2cta = st.sm_count / 2;
+        if (st.clusters_grouped <= 0) st.clusters_grouped = st.sm_count / 2;
+        if (st.ctas_1cta <= 0) st.ctas_1cta = st.sm_count;
+      }
+    }
+  }
+  *out = &st;
+  return st.init_status;
+}
+
+bool get_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dtype, uint64_t inner,
+             uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+             CUtensorMapSwizzle swizzle) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  MapKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.ptr = ptr;
+  key.inner = inner;
+  key.outer = outer;
+  key.row_bytes = row_bytes;
+  key.box_inner = box_inner;
+  key.box_outer = box_outer;
+  key.dtype = static_cast<int>(dtype);
+  key.swizzle = static_cast<int>(swizzle);
+  key.device = dev;
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = g_maps.find(key);
+  if (it != g_maps.end()) {
+    *m = it->second;
+    return true;
+  }
+  cuuint64_t gdim[2] = {inner, outer};
+  cuuint64_t gstride[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estride[2] = {1, 1};
+  CUtensorMap map;
+  if (g_encode(&map, dtype, 2, const_cast<void*>(ptr), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  if (g_maps.size() > 8192) g_maps.clear();
+  g_maps.emplace(key, map);
+  *m = map;
+  return true;
+}
+
+int force_kernel_from_env() {
+  const char* v = std::getenv("BWG_FORCE_KERNEL");
+  if (v == nullptr) return 0;
+  if (!std::strcmp(v, "1cta")) return BWG_KERNEL_1CTA;
+  if (!std::strcmp(v, "2cta")) return BWG_KERNEL_2CTA;
+  if (!std::strcmp(v, "small_m")) return BWG_KERNEL_SMALL_M;
+  return 0;
+}
+
+int force_stages_from_env() {
+  const char* v = std::getenv("BWG_FORCE_STAGES");
+  return v ? std::atoi(v) : 0;
+}
+
+CUtensorMapDataType out_map_dtype(int out_dtype) {
+  if (out_dtype == BWG_OUT_FP32) return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  if (out_dtype == BWG_OUT_FP16) return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
+
+bwg_status launch_status(cudaError_t e) {
+  if (e == cudaSuccess) return BWG_OK;
+  cudaGetLastError();
+  return BWG_ERR_CUDA;
+}
+
+bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M, int N, int K,
+                     int lda, int ldb, int ldd, int out_dtype, cudaStream_t stream) {
+  bwg_status s = check_args(A, B, D, M, N, K, lda, ldb, ldd, out_dtype);
+  if (s != BWG_OK) return s;
+  if (M == 0 || N == 0) return BWG_OK;
+  DeviceState* st = nullptr;
+  if ((s = ensure_device(&st)) != BWG_OK) return s;
+  bwg_plan_info pl;
+  s = plan_dense(M, N, K, out_dtype, fp16_in, st->sm_count, st->max_smem, force_kernel_from_env(),
+                 force_stages_from_env(), st->clusters_2cta, st->ctas_1cta, &pl);
+  if (s != BWG_OK) return s;
+  if (pl.kernel == BWG_KERNEL_ZERO)
+    return launch_status(launch_zero_fill(D, M, N, ldd, out_elt(out_dtype), stream));
+  const CUtensorMapDataType in_t =
+      fp16_in ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int oe = out_elt(out_dtype);
+  if (pl.kernel == BWG_KERNEL_SMALL_M) {
+    SmallMParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int m_pad = pl.mma_n;
+    if (!get_map(&p.map_bt, B, in_t, N, K, static_cast<uint64_t>(ldb) * 2, 64, kBK,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !get_map(&p.map_at, A, in_t, K, M, static_cast<uint64_t>(lda) * 2, kBK, m_pad,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !get_map(&p.map_d, D, out_map_dtype(out_dtype), N, M, static_cast<uint64_t>(ldd) * oe, 64,
+                 m_pad, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return BWG_ERR_CUDA;
+    p.err = st->err;
+    p.timeout_ns = g_timeout_ns.load();
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.m_pad = m_pad;
+    p.num_tiles = pl.tiles;
+    p.num_k_blocks = pl.k_blocks;
+    p.stages = pl.stages;
+    p.out_dtype = out_dtype;
+    p.idesc = pl.idesc;
+    p.tx_extra = g_tx_extra.load();
+    return launch_status(launch_small_m(p, pl.grid, pl.smem_total, stream));
+  }
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  const uint32_t d_box_inner = out_dtype == BWG_OUT_FP32 ? 32 : 64;
+  if (!get_map(&p.map_a, A, in_t, K, M, static_cast<uint64_t>(lda) * 2, kBK, kRowsPerCta,
+               CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !get_map(&p.map_b, B, in_t, N, K, static_cast<uint64_t>(ldb) * 2, 64, kBK,
+               CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !get_map(&p.map_d, D, out_map_dtype(out_dtype), N, M, static_cast<uint64_t>(ldd) * oe,
+               d_box_inner, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+    return BWG_ERR_CUDA;
+  p.err = st->err;
+  p.d_ptr = D;
+  p.timeout_ns = g_timeout_ns.load();
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.ldd = ldd;
+  p.num_m_tiles = ceil_div(M, pl.tile_m);
+  p.num_n_tiles = ceil_div(N, pl.tile_n);
+  p.num_k_blocks = pl.k_blocks;
+  p.group_m = kGroupM;
+  p.stages = pl.stages;
+  p.out_dtype = out_dtype;
+  p.idesc = pl.idesc;
+  p.tx_extra = g_tx_extra.load();
+  if (pl.kernel == BWG_KERNEL_2CTA)
+    return launch_status(launch_gemm_2cta(p, pl.grid, pl.smem_total, stream));
+  return launch_status(launch_gemm_1cta(p, pl.grid, pl.smem_total, stream));
+}
+
+bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
+                       const int* group_offsets, int G, int M_total, int N, int K,
+                       cudaStream_t stream) {
+  if (G < 0 || M_total < 0 || N < 0 || K < 0) return BWG_ERR_INVALID_ARG;
+  if (G == 0 || M_total == 0 || N == 0) return BWG_OK;
+  if (D == nullptr || group_offsets == nullptr) return BWG_ERR_INVALID_ARG;
+  if (!aligned16(D) || (static_cast<long long>(N) * 2) % 16 != 0) return BWG_ERR_ALIGNMENT;
+  if (K > 0) {
+    if (A == nullptr || B == nullptr) return BWG_ERR_INVALID_ARG;
+    if (!aligned16(A) || (static_cast<long long>(K) * 2) % 16 != 0) return BWG_ERR_ALIGNMENT;
+    for (int g = 0; g < G; ++g) {
+      if (B[g] == nullptr) return BWG_ERR_INVALID_ARG;
+      if (!aligned16(B[g])) return BWG_ERR_ALIGNMENT;
+    }
+  }
+  DeviceState* st = nullptr;
+  bwg_status s = ensure_device(&st);
+  if (s != BWG_OK) return s;
+  if (K == 0) return launch_status(launch_zero_fill(D, M_total, N, N, 2, stream));
+  const CUtensorMapDataType in_t =
+      fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int stages = force_stages_from_env() > 0 ? force_stages_from_env() : 6;
+  const int smem = dense_smem(2, stages);
+  if (smem > st->max_smem) return BWG_ERR_UNSUPPORTED;
+  for (int g0 = 0; g0 < G; g0 += kMaxGroupsPerLaunch) {
+    const int gn = std::min(kMaxGroupsPerLaunch, G - g0);
+    GroupedParams P;
+    std::memset(&P, 0, sizeof(P));
+    GemmParams& p = P.base;
+    if (!get_map(&p.map_a, A, in_t, K, M_total, static_cast<uint64_t>(K) * 2, kBK, kRowsPerCta,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !get_map(&p.map_d, D, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                 N, M_total, static_cast<uint64_t>(N) * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+      return BWG_ERR_CUDA;
+    for (int i = 0; i < gn; ++i)
+      if (!get_map(&P.map_b[i], B[g0 + i], in_t, N, K, static_cast<uint64_t>(N) * 2, 64, kBK,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return BWG_ERR_CUDA;
+    p.err = st->err;
+    p.d_ptr = D;
+    p.group_offsets = group_offsets;
+    p.timeout_ns = g_timeout_ns.load();
+    p.M = M_total;
+    p.N = N;
+    p.K = K;
+    p.ldd = N;
+    p.num_n_tiles = ceil_div(N, kTileN);
+    p.num_m_tiles = 0;
+    p.num_k_blocks = ceil_div(K, kBK);
+    p.group_m = kGroupM;
+    p.stages = stages;
+    p.out_dtype = fp16 ? BWG_OUT_FP16 : BWG_OUT_BF16;
+    p.idesc = make_idesc_f16(fp16 ? kFmtF16 : kFmtBF16, false, true, 2 * kRowsPerCta, kTileN);
+    p.tx_extra = g_tx_extra.load();
+    p.G = gn;
+    p.g_begin = g0;
+    p.G_total = G;
+    // Upper bound on tiles: every group adds at most one partial row tile.
+    const long long max_tiles =
+        (static_cast<long long>(ceil_div(M_total, 2 * kRowsPerCta)) + gn) * p.num_n_tiles;
+    const int clusters = static_cast<int>(std::min<long long>(max_tiles, st->clusters_grouped));
+    const cudaError_t e = launch_grouped_2cta(P, 2 * clusters, smem, stream);
+    if (e != cudaSuccess) return launch_status(e);
+  }
+  return BWG_OK;
+}
+
+}  // namespace
+
+// ================================================================ C ABI ====
+
+extern "C" {
+
+bwg_status gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K, int lda, int ldb,
+                     int ldd, int out_dtype, void* stream) {
+  return run_dense(false, A, B, D, M, N, K, lda, ldb, ldd, out_dtype,
+                   static_cast<cudaStream_t>(stream));
+}
+
+bwg_status gemm_fp16(const void* A, const void* B, void* D, int M, int N, int K, int lda, int ldb,
+                     int ldd, int out_dtype, void* stream) {
+  return run_dense(true, A, B, D, M, N, K, lda, ldb, ldd, out_dtype,
+                   static_cast<cudaStream_t>(stream));
+}
+
+bwg_status grouped_gemm_bf16(const void* A, const void* const* B, void* D, const int* group_offsets,
+                             int G, int M_total, int N, int K, void* stream) {
+  return run_grouped(false, A, B, D, group_offsets, G, M_total, N, K,
+                     static_cast<cudaStream_t>(stream));
+}
+
+bwg_status grouped_gemm_fp16(const void* A, const void* const* B, void* D, const int* group_offsets,
+                             int G, int M_total, int N, int K, void* stream) {
+  return run_grouped(true, A, B, D, group_offsets, G, M_total, N, K,
+                     static_cast<cudaStream_t>(stream));
+}
+
+bwg_status gemm_bf16_host(const void* A_host, const void* B_host, void* D_host, int M, int N, int K,
+                          int out_dtype, void* dA, void* dB, void* dD, void* stream) {
+  if (M < 0 || N < 0 || K < 0) return BWG_ERR_INVALID_ARG;
+  if (M > 0 && N > 0 && (D_host == nullptr || (K > 0 && (A_host == nullptr || B_host == nullptr))))
+    return BWG_ERR_INVALID_ARG;
+  bwg_status s = check_args(dA, dB, dD, M, N, K, K, N, N, out_dtype);
+  if (s != BWG_OK || M == 0 || N == 0) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t a_bytes = static_cast<size_t>(M) * K * 2, b_bytes = static_cast<size_t>(K) * N * 2;
+  const size_t d_bytes = static_cast<size_t>(M) * N * out_elt(out_dtype);
+  if (K > 0 && (cudaMemcpyAsync(dA, A_host, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+                cudaMemcpyAsync(dB, B_host, b_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess))
+    return launch_status(cudaErrorUnknown);
+  s = run_dense(false, dA, dB, dD, M, N, K, K, N, N, out_dtype, st);
+  if (s != BWG_OK) return s;
+  return launch_status(cudaMemcpyAsync(D_host, dD, d_bytes, cudaMemcpyDeviceToHost, st));
+}
+
+const char* bwg_status_string(int status) {
+  switch (status) {
+    case BWG_OK: return "ok";
+    case BWG_ERR_INVALID_ARG: return "invalid argument";
+    case BWG_ERR_ALIGNMENT: return "pointer or leading dimension not 16-byte aligned";
+    case BWG_ERR_UNSUPPORTED: return "unsupported device or size";
+    case BWG_ERR_CUDA: return "CUDA runtime or driver error";
+    case BWG_ERR_TIMEOUT: return "kernel barrier wait timed out";
+    default: return "unknown status";
+  }
+}
+
+bwg_status bwg_last_device_error(void* stream, unsigned long long* info) {
+  if (info == nullptr) return BWG_ERR_INVALID_ARG;
+  *info = 0;
+  DeviceState* st = nullptr;
+  bwg_status s = ensure_device(&st);
+  if (s != BWG_OK) return s;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return launch_status(cudaErrorUnknown);
+  unsigned long long w = 0;
+  if (cudaMemcpy(&w, st->err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(st->err, 0, sizeof(w)) != cudaSuccess)
+    return launch_status(cudaErrorUnknown);
+  *info = w;
+  const unsigned long long kind = w >> 56;
+  if (kind == kFaultTimeout) return BWG_ERR_TIMEOUT;
+  if (kind == kFaultBadOffsets) return BWG_ERR_INVALID_ARG;
+  return BWG_OK;
+}
+
+void bwg_set_watchdog_ns(unsigned long long ns) { g_timeout_ns.store(ns ? ns : 2000000000ull); }
+
+void bwg_debug_set_tx_extra(unsigned int bytes) { g_tx_extra.store(bytes); }
+
+bwg_status bwg_plan(int M, int N, int K, int out_dtype, int sm_count, int force_kernel,
+                    int force_stages, bwg_plan_info* out) {
+  if (out == nullptr || M < 0 || N < 0 || K < 0 || sm_count <= 0) return BWG_ERR_INVALID_ARG;
+  if (out_dtype != BWG_OUT_BF16 && out_dtype != BWG_OUT_FP32 && out_dtype != BWG_OUT_FP16)
+    return BWG_ERR_INVALID_ARG;
+  // 227 KiB of opt-in shared memory per block on sm_100-family parts.
+  return plan_dense(M, N, K, out_dtype, false, sm_count, 232448, force_kernel, force_stages, 0, 0,
+                    out);
+}
+
+bwg_status bwg_check_gemm_args(const void* A, const void* B, const void* D, int M, int N, int K,
+                               int lda, int ldb, int ldd, int out_dtype) {
+  return check_args(A, B, D, M, N, K, lda, ldb, ldd, out_dtype);
+}
+
+uint32_t bwg_idesc_f16(int bf16, int a_mn_major, int b_mn_major, int m, int n) {
+  return make_idesc_f16(bf16 ? kFmtBF16 : kFmtF16, a_mn_major != 0, b_mn_major != 0,
+                        static_cast<uint32_t>(m), static_cast<uint32_t>(n));
+}
+
+uint64_t bwg_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes, int swizzle) {
+  return make_smem_desc(smem_addr, lbo_bytes, sbo_bytes, static_cast<uint32_t>(swizzle));
+}
+
+uint32_t bwg_swizzle128_offset(uint32_t row, uint32_t chunk) { return swizzle128_offset(row, chunk); }
+
+void bwg_raster_tile(int t, int num_m_tiles, int num_n_tiles, int group_m, int* m_tile,
+                     int* n_tile) {
+  raster_tile(t, num_m_tiles, num_n_tiles, group_m, m_tile, n_tile);
+}
+
+int bwg_grouped_schedule(const int* offsets, int G, int M_total, int N, int tile_m, int* prefix,
+                         int* lo, int* hi) {
+  return grouped_tables(offsets, 0, G, G, M_total, ceil_div(N, kTileN), tile_m, prefix, lo, hi) ? 1
+                                                                                                 : 0;
+}
+
+void bwg_grouped_tile(int t, int G, const int* prefix, const int* lo, const int* hi, int tile_m,
+                      int* g, int* m0, int* n0, int* row_end) {
+  grouped_tile(t, G, prefix, lo, hi, tile_m, kTileN, g, m0, n0, row_end);
+}
+
+const char* bwg_version(void) { return "bwgemm 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,470 @@
+// Persistent, warp-specialised BF16/FP16 GEMM on tcgen05 tensor cores (sm_103a).
+//
+//   D[M,N] = A[M,K] x B[K,N],  A row-major (K-major operand), B row-major
+//   (N-major operand), FP32 accumulation in TMEM, BF16/FP16/FP32 output.
+//
+// Structure (the design the pages walk through, re-derived for this library):
+//  - "使用 Warp Specialization 和 Cluster 扩展 GEMM", step 7: one TMA producer
+//    warp, one MMA issuer warp, a warpgroup of epilogue warps, joined by four
+//    barrier kinds (SMEM full/empty ring, accumulator full/empty) with
+//    producer/consumer phases that start opposite.
+//  - same page, step 8: a CTA pair computes a 256x256 tile with
+//    tcgen05.mma.cta_group::2; each CTA loads its own 128 rows of A and its own
+//    128 columns of B; CTA 0's barrier collects both CTAs' TMA bytes; commits
+//    reach both CTAs with CTA mask 0b11; the accumulator-empty barrier in CTA 0
+//    collects the epilogue arrivals of both CTAs.
+//  - "B200 的 2CTA 怎样调优", section 七: two accumulator slots of 128x256 FP32
+//    per CTA (512 TMEM columns), so the epilogue of tile p overlaps the MMA of
+//    tile p+1.
+//  - "GEMM优化（三）", sections 3.2-3.4: a grouped raster order of output tiles
+//    so that concurrently running tiles share A row-strips and B column-strips
+//    in L2.
+//
+// Differences from the pages' kernels: B is consumed in its natural [K,N]
+// row-major layout as an MN-major operand (the pages store B as [N,K]); the
+// epilogue stages 32-row boxes per warp and issues one TMA store per warp, so
+// no warpgroup-wide named barrier is needed; each epilogue warp (not thread)
+// arrives once on the accumulator-empty barrier; every barrier wait is bounded
+// in time and reports a fault word instead of hanging.
+#include "layout.h"
+#include "params.h"
+#include "ptx.cuh"
+
+namespace bwg {
+namespace {
+
+constexpr uint32_t kAStageBytes = kRowsPerCta * kBK * 2;  // 16 KiB: 128 rows x 64 K
+constexpr uint32_t kBChunkBytes = 64 * kBK * 2;           // 8 KiB: 64 K rows x 64 N
+
+enum : uint32_t { kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2 };
+enum : uint32_t { kBarFull = 0, kBarEmpty = 1, kBarAccFull = 2, kBarAccEmpty = 3 };
+
+__device__ __forceinline__ void record_fault(unsigned long long* err, unsigned long long kind,
+                                             uint32_t role, uint32_t bar, uint32_t stage,
+                                             uint32_t phase) {
+  const unsigned long long code = (kind << 56) | (static_cast<unsigned long long>(role) << 48) |
+                                  (static_cast<unsigned long long>(bar) << 40) |
+                                  (static_cast<unsigned long long>(blockIdx.x & 0xFFFFFFu) << 16) |
+                                  ((stage & 0xFFu) << 8) | (phase & 0xFFu);
+  atomicCAS(err, 0ull, code);
+}
+
+// One output tile of the cluster: first row (of the pair), first column, the
+// row bound for stores (M, or the end of the tile's group) and the group.
+struct Tile {
+  int m0;
+  int n0;
+  int row_end;
+  int g;
+};
+
+template <int CG, bool GROUPED>
+struct Sched {
+  static constexpr int kTileM = kRowsPerCta * CG;
+  const GemmParams& p;
+  const int* prefix;  // grouped tables in shared memory: prefix[G+1], lo[G], hi[G]
+  const int* lo;
+  const int* hi;
+
+  __device__ int total() const {
+    if constexpr (GROUPED)
+      return prefix[p.G];
+    else
+      return p.num_m_tiles * p.num_n_tiles;
+  }
+
+  __device__ Tile at(int t) const {
+    Tile tl;
+    if constexpr (GROUPED) {
+      grouped_tile(t, p.G, prefix, lo, hi, kTileM, kTileN, &tl.g, &tl.m0, &tl.n0, &tl.row_end);
+    } else {
+      int mt, nt;
+      raster_tile(t, p.num_m_tiles, p.num_n_tiles, p.group_m, &mt, &nt);
+      tl.m0 = mt * kTileM;
+      tl.n0 = nt * kTileN;
+      tl.row_end = p.M;
+      tl.g = 0;
+    }
+    return tl;
+  }
+};
+
+// Warp-uniform bounded wait: every lane waits, and the warp proceeds only if
+// all lanes saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const bool ok = mbar_wait(bar, parity, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int CG, bool GROUPED, class PT>
+__device__ __forceinline__ const CUtensorMap* b_map(const PT& P, int g) {
+  if constexpr (GROUPED)
+    return &P.map_b[g];
+  else
+    return &P.map_b;
+}
+
+template <int CG, bool GROUPED, class PT>
+__device__ void gemm_body(const PT& P, const GemmParams& p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+  const int S = p.stages;
+  constexpr uint32_t kBCols = kTileN / CG;             // B columns this CTA loads
+  constexpr uint32_t kBStageBytes = kBCols * kBK * 2;  // 32 KiB (1 CTA) or 16 KiB (pair)
+  constexpr uint32_t kBChunks = kBCols / 64;
+
+  const uint32_t smem_a = base;
+  const uint32_t smem_b = smem_a + S * kAStageBytes;
+  const uint32_t smem_epi = smem_b + S * kBStageBytes;
+  const uint32_t smem_bar = smem_epi + kEpiBytes;
+  auto full_bar = [&](int s) { return smem_bar + 8u * s; };
+  auto empty_bar = [&](int s) { return smem_bar + 8u * (S + s); };
+  auto acc_full_bar = [&](int a) { return smem_bar + 8u * (2 * S + a); };
+  auto acc_empty_bar = [&](int a) { return smem_bar + 8u * (2 * S + 2 + a); };
+  const uint32_t tmem_slot = smem_bar + 8u * (2 * S + 4);
+  const uint32_t tables = tmem_slot + 16u;
+
+  // ---- set-up: barriers, grouped tables, TMEM allocation -----------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(acc_full_bar(a), 1);
+      mbar_init(acc_empty_bar(a), CG * 4);
+    }
+    fence_mbarrier_init();
+  }
+  // Grouped tables live after the barriers, in shared memory (generic pointers).
+  int* tab = reinterpret_cast<int*>(smem_raw + (tables - smem_u32(smem_raw)));
+  int* t_prefix = tab;
+  int* t_lo = tab + kMaxGroupsPerLaunch + 1;
+  int* t_hi = t_lo + kMaxGroupsPerLaunch;
+  if constexpr (GROUPED) {
+    if (threadIdx.x == 64) {
+      const bool ok = grouped_tables(p.group_offsets, p.g_begin, p.G, p.G_total, p.M,
+                                     p.num_n_tiles, kRowsPerCta * CG, t_prefix, t_lo, t_hi);
+      if (!ok && rank == 0) record_fault(p.err, kFaultBadOffsets, 0, 0, 0, 0);
+    }
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&p.map_a);
+    prefetch_tensormap(&p.map_d);
+    if constexpr (!GROUPED) prefetch_tensormap(&p.map_b);
+  }
+  if (warp == 1) {
+    tmem_alloc<CG>(tmem_slot, kTmemCols);
+    tmem_relinquish<CG>();
+  }
+  tc_fence_before();
+  if constexpr (CG == 2)
+    cluster_sync_all();
+  else
+    __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ld_shared_u32(tmem_slot);
+
+  const Sched<CG, GROUPED> sched{p, t_prefix, t_lo, t_hi};
+  const int total = sched.total();
+  const int first = static_cast<int>((CG == 2) ? cluster_id_x() : blockIdx.x);
+  const int stride = static_cast<int>((CG == 2) ? num_clusters_x() : gridDim.x);
+  bool aborted = false;
+
+  if (warp == 0) {
+    // ---- TMA producer: one thread streams A and B k-blocks into the ring ----
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      const uint32_t stage_tx = CG * (kAStageBytes + kBStageBytes) + p.tx_extra;
+      for (int t = first; t < total && !aborted; t += stride) {
+        const Tile tl = sched.at(t);
+        const int a_row = tl.m0 + static_cast<int>(rank) * kRowsPerCta;
+        const int b_col = tl.n0 + static_cast<int>(rank * kBCols);
+        const CUtensorMap* mb = b_map<CG, GROUPED>(P, tl.g);
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, p.timeout_ns)) {
+            record_fault(p.err, kFaultTimeout, kRoleProducer, kBarEmpty, s, ph ^ 1u);
+            aborted = true;
+            break;
+          }
+          const uint32_t sa = smem_a + s * kAStageBytes;
+          const uint32_t sb = smem_b + s * kBStageBytes;
+          const int k0 = kb * kBK;
+          if constexpr (CG == 2) {
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(s), stage_tx);
+            const uint32_t fb = mapa_shared(full_bar(s), 0);
+            tma_load_2d_pair(sa, &p.map_a, fb, k0, a_row);
+#pragma unroll
+            for (uint32_t j = 0; j < kBChunks; ++j)
+              tma_load_2d_pair(sb + j * kBChunkBytes, mb, fb, b_col + 64 * j, k0);
+          } else {
+            mbar_arrive_expect_tx(full_bar(s), stage_tx);
+            tma_load_2d(sa, &p.map_a, full_bar(s), k0, a_row);
+#pragma unroll
+            for (uint32_t j = 0; j < kBChunks; ++j)
+              tma_load_2d(sb + j * kBChunkBytes, mb, full_bar(s), b_col + 64 * j, k0);
+          }
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---- MMA issuer: one thread of CTA 0 drives the tensor cores -----------
+    if (rank == 0 && lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      for (int t = first; t < total && !aborted; t += stride) {
+        if (!mbar_wait(acc_empty_bar(acc), acc_ph ^ 1u, p.timeout_ns)) {
+          record_fault(p.err, kFaultTimeout, kRoleMma, kBarAccEmpty, acc, acc_ph ^ 1u);
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * kTileN;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait(full_bar(s), ph, p.timeout_ns)) {
+            record_fault(p.err, kFaultTimeout, kRoleMma, kBarFull, s, ph);
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t a_desc = make_smem_desc(smem_a + s * kAStageBytes, 16, 1024, kSwizzle128B);
+          const uint64_t b_desc =
+              make_smem_desc(smem_b + s * kBStageBytes, kBChunkBytes, 1024, kSwizzle128B);
+#pragma unroll
+          for (uint32_t kk = 0; kk < kBK / 16; ++kk) {
+            // K-major A: the next 16 K values are 32 bytes further along each
+            // 128-byte row.  MN-major B: they are 16 rows (2048 bytes) further.
+            mma_f16<CG>(d_tmem, a_desc + ((kk * 32u) >> 4), b_desc + ((kk * 2048u) >> 4), p.idesc,
+                        (kb | kk) != 0 ? 1u : 0u);
+          }
+          if constexpr (CG == 2)
+            mma_commit_pair_mc(empty_bar(s), 0x3);
+          else
+            mma_commit_1cta(empty_bar(s));
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (aborted) break;
+        if constexpr (CG == 2)
+          mma_commit_pair_mc(acc_full_bar(acc), 0x3);
+        else
+          mma_commit_1cta(acc_full_bar(acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_ph ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue: TMEM -> registers -> convert -> swizzled SMEM -> TMA -----
+    const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may read
+    const uint32_t ebuf = smem_epi + (warp - 2u) * 2u * kEpiBufBytes;
+    const uint32_t acc_empty_leader0 = (CG == 2) ? mapa_shared(acc_empty_bar(0), 0) : acc_empty_bar(0);
+    const bool out32 = p.out_dtype == kOutF32;
+    const bool outbf = p.out_dtype == kOutBF16;
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    uint32_t buf = 0;
+    for (int t = first; t < total; t += stride) {
+      const Tile tl = sched.at(t);
+      if (!warp_wait(acc_full_bar(acc), acc_ph, p.timeout_ns)) {
+        if (lane == 0) record_fault(p.err, kFaultTimeout, kRoleEpilogue, kBarAccFull, acc, acc_ph);
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const int row_w = tl.m0 + static_cast<int>(rank * kRowsPerCta + q * 32u);
+      const uint32_t t_acc = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc) * kTileN;
+      const int sub_cols = out32 ? 32 : 64;
+      const int nsub = kTileN / sub_cols;
+      for (int sub = 0; sub < nsub; ++sub) {
+        uint32_t pk[32];
+        if (out32) {
+          tmem_ld_32x32b_x32(t_acc + sub * 32, pk);
+          tmem_wait_ld();
+        } else {
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(t_acc + sub * 64, v0);
+          tmem_ld_32x32b_x32(t_acc + sub * 64 + 32, v1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float lo0 = __uint_as_float(v0[2 * i]), hi0 = __uint_as_float(v0[2 * i + 1]);
+            const float lo1 = __uint_as_float(v1[2 * i]), hi1 = __uint_as_float(v1[2 * i + 1]);
+            pk[i] = outbf ? pack_bf16x2(lo0, hi0) : pack_f16x2(lo0, hi0);
+            pk[16 + i] = outbf ? pack_bf16x2(lo1, hi1) : pack_f16x2(lo1, hi1);
+          }
+        }
+        if (sub == nsub - 1) {
+          // Last TMEM read of this accumulator: hand it back to the MMA warp.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
+        }
+        const int col0 = tl.n0 + sub * sub_cols;
+        if (col0 >= p.N) continue;
+        const bool whole_box = !GROUPED || (row_w + 32 <= tl.row_end);
+        if (whole_box) {
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+          const uint32_t sb = ebuf + buf * kEpiBufBytes;
+#pragma unroll
+          for (uint32_t j = 0; j < 8; ++j)
+            st_shared_v4(sb + swizzle128_offset(lane, j), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                         pk[4 * j + 3]);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.map_d, sb, col0, row_w);
+            bulk_commit_group();
+          }
+          buf ^= 1u;
+        } else {
+          // Ragged end of a group: each thread stores its own row, if inside.
+          const int row = row_w + static_cast<int>(lane);
+          if (row < tl.row_end) {
+            const int elt = out32 ? 4 : 2;
+            uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) +
+                            (static_cast<size_t>(row) * p.ldd + col0) * elt;
+            const int ncols = min(sub_cols, p.N - col0);
+            if (ncols == sub_cols) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                reinterpret_cast<uint4*>(drow)[j] =
+                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            } else if (out32) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                if (c < ncols) reinterpret_cast<uint32_t*>(drow)[c] = pk[c];
+            } else {
+#pragma unroll
+              for (int c = 0; c < 64; ++c)
+                if (c < ncols)
+                  reinterpret_cast<uint16_t*>(drow)[c] =
+                      static_cast<uint16_t>(pk[c >> 1] >> ((c & 1) * 16));
+            }
+          }
+        }
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_ph ^= 1u;
+      }
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  // ---- teardown -----------------------------------------------------------
+  if (__syncthreads_or(aborted ? 1 : 0)) {
+    // A wait gave up: give copies already in flight time to land before the
+    // shared memory and TMEM they target are released.
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 200000ull) nanosleep_ns(1000);
+  }
+  tc_fence_before();
+  if constexpr (CG == 2)
+    cluster_sync_all();
+  else
+    __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<CG>(tmem_base, kTmemCols);
+  }
+}
+
+template <int CG>
+__global__ void __launch_bounds__(kThreads, 1) gemm_dense_kernel(const __grid_constant__ GemmParams p) {
+  gemm_body<CG, false>(p, p);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_grouped_kernel(const __grid_constant__ GroupedParams p) {
+  gemm_body<2, true>(p, p.base);
+}
+
+template <class K, class P>
+cudaError_t launch_cluster(K kernel, const P& p, int cg, int grid, size_t smem, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cg);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_1cta(const GemmParams& p, int grid, size_t smem, cudaStream_t s) {
+  return launch_cluster(gemm_dense_kernel<1>, p, 1, grid, smem, s);
+}
+
+cudaError_t launch_gemm_2cta(const GemmParams& p, int grid, size_t smem, cudaStream_t s) {
+  return launch_cluster(gemm_dense_kernel<2>, p, 2, grid, smem, s);
+}
+
+cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, cudaStream_t s) {
+  return launch_cluster(gemm_grouped_kernel, p, 2, grid, smem, s);
+}
+
+static int occupancy_clusters(const void* fn, int cg, size_t smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cg), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cg);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+int max_active_clusters_gemm(int cg, bool grouped, size_t smem) {
+  const void* fn = grouped ? reinterpret_cast<const void*>(gemm_grouped_kernel)
+                           : (cg == 2 ? reinterpret_cast<const void*>(gemm_dense_kernel<2>)
+                                      : reinterpret_cast<const void*>(gemm_dense_kernel<1>));
+  return occupancy_clusters(fn, cg, smem);
+}
+
+cudaError_t set_gemm_attributes(size_t smem) {
+  const void* fns[3] = {reinterpret_cast<const void*>(gemm_dense_kernel<1>),
+                        reinterpret_cast<const void*>(gemm_dense_kernel<2>),
+                        reinterpret_cast<const void*>(gemm_grouped_kernel)};
+  for (const void* fn : fns) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace bwg

@@ -1,0 +1,119 @@
+// Bit layouts shared by the host planner/tests and the kernels:
+//  - the tcgen05.mma instruction descriptor for kind::f16,
+//  - the tcgen05 shared-memory matrix descriptor,
+//  - the 128-byte swizzle that TMA applies to a tile in shared memory.
+//
+// Field positions follow the public PTX ISA (tcgen05 "Instruction descriptor"
+// and "Shared memory descriptor" tables).  The MegaMoE page ("MegaMoE …
+// 融合算子解读", section 04, dynamic N) prints one of these fields itself: the
+// N extent enters the instruction descriptor as (N >> 3) << 17.
+#pragma once
+
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define BWG_HD __host__ __device__ __forceinline__
+#else
+#define BWG_HD inline
+#endif
+
+namespace bwg {
+
+// Operand formats of kind::f16 (A and B must share one of these).
+constexpr uint32_t kFmtF16 = 0;
+constexpr uint32_t kFmtBF16 = 1;
+
+// Instruction descriptor, kind::f16, FP32 accumulator:
+//   [4,6)  D format (1 = F32)       [7,10) A format     [10,13) B format
+//   15     A is MN-major            16     B is MN-major
+//   [17,23) N >> 3                  [24,29) M >> 4
+BWG_HD uint32_t make_idesc_f16(uint32_t ab_fmt, bool a_mn_major, bool b_mn_major, uint32_t m,
+                               uint32_t n) {
+  return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// Swizzle modes of the shared-memory descriptor (bits 61..63).
+constexpr uint32_t kSwizzleNone = 0;
+constexpr uint32_t kSwizzle128B = 2;
+
+// Shared-memory matrix descriptor:
+//   [0,14)  start address >> 4      [16,30) leading byte offset >> 4
+//   [32,46) stride byte offset >> 4 [46,48) version (1 for tcgen05)
+//   [49,52) base offset (0: tiles are 1024-byte aligned)   [61,64) swizzle
+BWG_HD uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                               uint32_t swizzle) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
+         (static_cast<uint64_t>(swizzle & 7u) << 61);
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a tile whose
+// rows are 128 bytes and which TMA wrote with 128-byte swizzle: the chunk index
+// is XOR-ed with the row index modulo 8 ("GEMM优化（三）", section 2.1).
+BWG_HD uint32_t swizzle128_offset(uint32_t row, uint32_t chunk) {
+  return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+// Grouped raster order of output tiles ("GEMM优化（三）", section 3.2-3.4):
+// tiles are taken in groups of `group_m` tile rows; inside a group the row
+// index runs fastest, so the tiles in flight at one time share a few B column
+// strips and `group_m` A row strips, which then stay in L2.
+BWG_HD void raster_tile(int t, int num_m_tiles, int num_n_tiles, int group_m, int* m_tile,
+                        int* n_tile) {
+  const int gsz = group_m * num_n_tiles;
+  const int grp = t / gsz;
+  const int first_m = grp * group_m;
+  const int rows = (num_m_tiles - first_m) < group_m ? (num_m_tiles - first_m) : group_m;
+  const int r = t - grp * gsz;
+  *m_tile = first_m + r % rows;
+  *n_tile = r / rows;
+}
+
+// Grouped (expert) schedule.  From the offsets of groups g0 .. g0+G-1 build
+//   prefix[g] = tiles of groups before g (prefix[G] = all tiles),
+//   lo[g], hi[g] = the group's row range, clamped into [0, M] and made
+//   non-decreasing so that no tile can reach outside A or D.
+// Returns true if the offsets honour the contract (first 0, non-decreasing,
+// inside [0, M], last == M when g0+G == G_total).
+BWG_HD bool grouped_tables(const int* offsets, int g0, int G, int G_total, int M, int num_n_tiles,
+                           int tile_m, int* prefix, int* lo, int* hi) {
+  bool ok = true;
+  int tiles = 0;
+  int prev_hi = 0;
+  for (int g = 0; g < G; ++g) {
+    int a = offsets[g0 + g];
+    int b = offsets[g0 + g + 1];
+    if (g0 + g == 0 && a != 0) ok = false;
+    if (b < a || a < prev_hi || a < 0 || b > M) ok = false;
+    a = a < prev_hi ? prev_hi : a;
+    a = a > M ? M : (a < 0 ? 0 : a);
+    b = b < a ? a : (b > M ? M : b);
+    prev_hi = b;
+    prefix[g] = tiles;
+    lo[g] = a;
+    hi[g] = b;
+    tiles += ((b - a + tile_m - 1) / tile_m) * num_n_tiles;
+  }
+  prefix[G] = tiles;
+  if (g0 + G == G_total && offsets[G_total] != M) ok = false;
+  return ok;
+}
+
+// Tile t of the grouped schedule: its group, first row, first column and the
+// group's row end.  Inside a group the row tile runs fastest, so the few
+// concurrently running tiles of one column strip share that strip of B_g.
+BWG_HD void grouped_tile(int t, int G, const int* prefix, const int* lo, const int* hi,
+                         int tile_m, int tile_n, int* g_out, int* m0, int* n0, int* row_end) {
+  int g = 0;
+  while (g + 1 < G && prefix[g + 1] <= t) ++g;  // prefix[g] <= t < prefix[g+1]
+  const int r = t - prefix[g];
+  const int mt = (hi[g] - lo[g] + tile_m - 1) / tile_m;
+  *g_out = g;
+  *m0 = lo[g] + (r % mt) * tile_m;
+  *n0 = (r / mt) * tile_n;
+  *row_end = hi[g];
+}
+
+}  // namespace bwg

@@ -1,0 +1,80 @@
+// Kernel parameter blocks (passed by value as __grid_constant__) and the
+// host-side launch entry points of each kernel translation unit.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace bwg {
+
+constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kBK = 64;              // K per stage: one 128-byte swizzle row of 16-bit data
+constexpr int kTileN = 256;          // output columns per tile (MMA N)
+constexpr int kRowsPerCta = 128;     // accumulator rows per CTA (TMEM lanes)
+constexpr int kEpiBufBytes = 4096;   // one 32-row x 128-byte staging box
+constexpr int kEpiBytes = 4 * 2 * kEpiBufBytes;  // 4 epilogue warps, double-buffered
+constexpr uint32_t kTmemCols = 512;  // two 256-column FP32 accumulators
+constexpr int kMaxGroupsPerLaunch = 64;
+constexpr int kSmallMMaxM = 128;     // swapped kernel handles up to 128 rows of A
+
+// Output element type codes (same values as the C ABI).
+constexpr int kOutBF16 = 0;
+constexpr int kOutF32 = 1;
+constexpr int kOutF16 = 2;
+
+// Device error word layout (written once per fault with atomicCAS from 0):
+//   [56,64) kind (1 = barrier wait timed out, 2 = invalid group offsets)
+//   [48,56) role (0 TMA producer, 1 MMA issuer, 2 epilogue)
+//   [40,48) barrier (0 full, 1 empty, 2 accumulator full, 3 accumulator empty)
+//   [16,40) block index      [8,16) stage      [0,8) phase parity
+constexpr unsigned long long kFaultTimeout = 1;
+constexpr unsigned long long kFaultBadOffsets = 2;
+
+struct GemmParams {
+  CUtensorMap map_a;  // A [rows, K] bf16/fp16, box {64 (K), 128 (rows)}, 128B swizzle
+  CUtensorMap map_b;  // B [K, N], box {64 (N), 64 (K)}, 128B swizzle (dense only)
+  CUtensorMap map_d;  // D [rows, N], box {64 or 32 (N), 32 (rows)}, 128B swizzle
+  unsigned long long* err;
+  void* d_ptr;               // D base, for masked row stores at ragged group ends
+  const int* group_offsets;  // grouped only: device int32 [G+1]
+  unsigned long long timeout_ns;
+  int M, N, K, ldd;          // M = rows of A and D (total rows for grouped)
+  int num_m_tiles, num_n_tiles, num_k_blocks;
+  int group_m;               // raster: tile rows per group of the grouped order
+  int stages;
+  int out_dtype;
+  uint32_t idesc;
+  uint32_t tx_extra;         // test hook: extra bytes expected per stage (0 normally)
+  int G, g_begin, G_total;   // grouped only: groups in this launch, first group, all groups
+};
+
+struct GroupedParams {
+  GemmParams base;
+  CUtensorMap map_b[kMaxGroupsPerLaunch];
+};
+
+struct SmallMParams {
+  CUtensorMap map_bt;  // B [K, N] viewed as the MMA's MN-major A: box {64 (N), 64 (K)}
+  CUtensorMap map_at;  // A [M, K] as the MMA's K-major B: box {64 (K), m_pad (rows)}
+  CUtensorMap map_d;   // D [M, N], box {64 (N), m_pad (rows)}, no swizzle
+  unsigned long long* err;
+  unsigned long long timeout_ns;
+  int M, N, K, m_pad;
+  int num_tiles, num_k_blocks, stages, out_dtype;
+  uint32_t idesc;
+  uint32_t tx_extra;
+};
+
+// Host launchers (one per kernel instantiation).  They only enqueue.
+cudaError_t launch_gemm_1cta(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_gemm_2cta(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_small_m(const SmallMParams& p, int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_zero_fill(void* d, int rows, int cols, int ld, int elt_bytes, cudaStream_t s);
+
+// Occupancy helpers: co-resident clusters (or CTAs) for a given launch shape.
+int max_active_clusters_gemm(int cg, bool grouped, size_t smem);
+int max_active_ctas_small_m(size_t smem);
+
+}  // namespace bwg

@@ -1,0 +1,240 @@
+"""Thin Python binding over libbwgemm.so (ctypes).
+
+Argument marshalling only: every function here converts torch tensors to
+device pointers, sizes and leading dimensions, calls the C ABI entry point of
+the same name and raises on a non-zero status.  All arithmetic runs in the
+library's CUDA kernels; if the library is missing or fails to load, every call
+raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbwgemm.so")
+
+OUT_BF16 = 0
+OUT_FP32 = 1
+OUT_FP16 = 2
+_OUT_CODES = {torch.bfloat16: OUT_BF16, torch.float32: OUT_FP32, torch.float16: OUT_FP16}
+
+KERNEL_NONE, KERNEL_ZERO, KERNEL_1CTA, KERNEL_2CTA, KERNEL_SMALL_M = range(5)
+
+STATUS_NAMES = {0: "BWG_OK", 1: "BWG_ERR_INVALID_ARG", 2: "BWG_ERR_ALIGNMENT",
+                3: "BWG_ERR_UNSUPPORTED", 4: "BWG_ERR_CUDA", 5: "BWG_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class BwgError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s failed: %s (%s)" % (what, STATUS_NAMES.get(status, status), status_string(status)))
+        self.status = status
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
+                ("tile_k", ctypes.c_int), ("mma_m", ctypes.c_int), ("mma_n", ctypes.c_int),
+                ("stages", ctypes.c_int), ("tiles", ctypes.c_int), ("k_blocks", ctypes.c_int),
+                ("coverage", ctypes.c_double), ("smem_input_per_cta", ctypes.c_int),
+                ("smem_total", ctypes.c_int), ("grid", ctypes.c_int), ("tx_bytes", ctypes.c_uint32),
+                ("idesc", ctypes.c_uint32)]
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it is not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libbwgemm.so is not built (%s); run __graft_entry__.build(). "
+                                   "There is no fallback implementation." % LIB_PATH)
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i, u32, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64
+            for name in ("gemm_bf16", "gemm_fp16"):
+                f = getattr(L, name)
+                f.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp]
+                f.restype = i
+            for name in ("grouped_gemm_bf16", "grouped_gemm_fp16"):
+                f = getattr(L, name)
+                f.argtypes = [vp, ctypes.POINTER(vp), vp, vp, i, i, i, i, vp]
+                f.restype = i
+            L.gemm_bf16_host.argtypes = [vp, vp, vp, i, i, i, i, vp, vp, vp, vp]
+            L.gemm_bf16_host.restype = i
+            L.bwg_status_string.argtypes = [i]
+            L.bwg_status_string.restype = ctypes.c_char_p
+            L.bwg_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_ulonglong)]
+            L.bwg_last_device_error.restype = i
+            L.bwg_set_watchdog_ns.argtypes = [ctypes.c_ulonglong]
+            L.bwg_set_watchdog_ns.restype = None
+            L.bwg_debug_set_tx_extra.argtypes = [ctypes.c_uint]
+            L.bwg_debug_set_tx_extra.restype = None
+            L.bwg_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(PlanInfo)]
+            L.bwg_plan.restype = i
+            L.bwg_check_gemm_args.argtypes = [vp, vp, vp, i, i, i, i, i, i, i]
+            L.bwg_check_gemm_args.restype = i
+            L.bwg_idesc_f16.argtypes = [i, i, i, i, i]
+            L.bwg_idesc_f16.restype = u32
+            L.bwg_smem_desc.argtypes = [u32, u32, u32, i]
+            L.bwg_smem_desc.restype = u64
+            L.bwg_swizzle128_offset.argtypes = [u32, u32]
+            L.bwg_swizzle128_offset.restype = u32
+            L.bwg_raster_tile.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+            L.bwg_raster_tile.restype = None
+            ip = ctypes.POINTER(i)
+            L.bwg_grouped_schedule.argtypes = [ip, i, i, i, i, ip, ip, ip]
+            L.bwg_grouped_schedule.restype = i
+            L.bwg_grouped_tile.argtypes = [i, i, ip, ip, ip, i, ip, ip, ip, ip]
+            L.bwg_grouped_tile.restype = None
+            L.bwg_version.argtypes = []
+            L.bwg_version.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().bwg_status_string(int(status)).decode()
+    except Exception:  # noqa: BLE001 - only used to format an error
+        return "?"
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise BwgError(status, what)
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _matrix(t: torch.Tensor, name: str) -> int:
+    if t.dim() != 2:
+        raise ValueError("%s must be 2-D" % name)
+    if t.stride(1) != 1:
+        raise ValueError("%s must be row-major with unit column stride" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    return t.stride(0)
+
+
+def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None,
+         out_dtype: torch.dtype = torch.bfloat16, stream=None) -> torch.Tensor:
+    """D = A @ B through gemm_bf16 / gemm_fp16 (chosen by A's dtype)."""
+    if A.dtype != B.dtype or A.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("A and B must both be bfloat16 or both float16")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ: %s x %s" % (tuple(A.shape), tuple(B.shape)))
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    if out.dtype not in _OUT_CODES:
+        raise TypeError("output dtype must be bfloat16, float16 or float32")
+    lda, ldb, ldd = _matrix(A, "A"), _matrix(B, "B"), _matrix(out, "out")
+    fn = gemm_bf16 if A.dtype == torch.bfloat16 else gemm_fp16
+    fn(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, lda, ldb, ldd, _OUT_CODES[out.dtype],
+       _stream_handle(stream, A.device))
+    return out
+
+
+def gemm_bf16(A_ptr: int, B_ptr: int, D_ptr: int, M: int, N: int, K: int, lda: int, ldb: int,
+              ldd: int, out_dtype: int, stream: int) -> None:
+    _check(lib().gemm_bf16(A_ptr, B_ptr, D_ptr, M, N, K, lda, ldb, ldd, out_dtype, stream), "gemm_bf16")
+
+
+def gemm_fp16(A_ptr: int, B_ptr: int, D_ptr: int, M: int, N: int, K: int, lda: int, ldb: int,
+              ldd: int, out_dtype: int, stream: int) -> None:
+    _check(lib().gemm_fp16(A_ptr, B_ptr, D_ptr, M, N, K, lda, ldb, ldd, out_dtype, stream), "gemm_fp16")
+
+
+def grouped_gemm(A: torch.Tensor, Bs: list, group_offsets: torch.Tensor,
+                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Grouped expert product through grouped_gemm_bf16 / grouped_gemm_fp16."""
+    if A.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("A must be bfloat16 or float16")
+    M_total, K = A.shape
+    G = len(Bs)
+    N = Bs[0].shape[1] if G else 0
+    for b in Bs:
+        if b.shape != (K, N) or b.dtype != A.dtype or not b.is_contiguous():
+            raise ValueError("every weight matrix must be a contiguous [K, N] tensor of A's dtype")
+    if group_offsets.dtype != torch.int32 or group_offsets.numel() != G + 1 or not group_offsets.is_cuda:
+        raise ValueError("group_offsets must be a CUDA int32 tensor with G+1 entries")
+    if not A.is_contiguous():
+        raise ValueError("A must be dense [M_total, K]")
+    if out is None:
+        out = torch.empty((M_total, N), dtype=A.dtype, device=A.device)
+    fn = grouped_gemm_bf16 if A.dtype == torch.bfloat16 else grouped_gemm_fp16
+    fn(A.data_ptr(), [b.data_ptr() for b in Bs], out.data_ptr(), group_offsets.data_ptr(), G, M_total,
+       N, K, _stream_handle(stream, A.device))
+    return out
+
+
+def _ptr_array(ptrs):
+    arr = (ctypes.c_void_p * max(len(ptrs), 1))(*[ctypes.c_void_p(p) for p in ptrs])
+    return ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)), arr
+
+
+def grouped_gemm_bf16(A_ptr: int, B_ptrs: list, D_ptr: int, offsets_ptr: int, G: int, M_total: int,
+                      N: int, K: int, stream: int) -> None:
+    p, keep = _ptr_array(B_ptrs)
+    _check(lib().grouped_gemm_bf16(A_ptr, p, D_ptr, offsets_ptr, G, M_total, N, K, stream),
+           "grouped_gemm_bf16")
+    del keep
+
+
+def grouped_gemm_fp16(A_ptr: int, B_ptrs: list, D_ptr: int, offsets_ptr: int, G: int, M_total: int,
+                      N: int, K: int, stream: int) -> None:
+    p, keep = _ptr_array(B_ptrs)
+    _check(lib().grouped_gemm_fp16(A_ptr, p, D_ptr, offsets_ptr, G, M_total, N, K, stream),
+           "grouped_gemm_fp16")
+    del keep
+
+
+def gemm_bf16_host(A_host: torch.Tensor, B_host: torch.Tensor, D_host: torch.Tensor,
+                   dA: torch.Tensor, dB: torch.Tensor, dD: torch.Tensor, stream=None) -> None:
+    """Host-buffer form: copies in, multiplies, copies out, all on `stream`."""
+    M, K = A_host.shape
+    N = B_host.shape[1]
+    if D_host.dtype not in _OUT_CODES:
+        raise TypeError("output dtype must be bfloat16, float16 or float32")
+    _check(lib().gemm_bf16_host(A_host.data_ptr(), B_host.data_ptr(), D_host.data_ptr(), M, N, K,
+                                _OUT_CODES[D_host.dtype], dA.data_ptr(), dB.data_ptr(), dD.data_ptr(),
+                                _stream_handle(stream, dA.device)), "gemm_bf16_host")
+
+
+def last_device_error(stream=None) -> tuple[int, int]:
+    """(status, raw error word) of the current device; clears the word."""
+    info = ctypes.c_ulonglong(0)
+    handle = _stream_handle(stream, torch.cuda.current_device()) if torch.cuda.is_available() else 0
+    st = lib().bwg_last_device_error(handle, ctypes.byref(info))
+    return st, info.value
+
+
+def set_watchdog_ns(ns: int) -> None:
+    lib().bwg_set_watchdog_ns(int(ns))
+
+
+def debug_set_tx_extra(nbytes: int) -> None:
+    lib().bwg_debug_set_tx_extra(int(nbytes))
+
+
+def plan(M: int, N: int, K: int, out_dtype: int = OUT_BF16, sm_count: int = 152,
+         force_kernel: int = 0, force_stages: int = 0) -> PlanInfo:
+    info = PlanInfo()
+    _check(lib().bwg_plan(M, N, K, out_dtype, sm_count, force_kernel, force_stages, ctypes.byref(info)),
+           "bwg_plan")
+    return info
+
+
+def check_gemm_args(A: int, B: int, D: int, M: int, N: int, K: int, lda: int, ldb: int, ldd: int,
+                    out_dtype: int) -> int:
+    return int(lib().bwg_check_gemm_args(A, B, D, M, N, K, lda, ldb, ldd, out_dtype))

@@ -1,0 +1,202 @@
+/*
+ * bwgemm: half-precision GEMM on one GB300 (sm_103a) -- C ABI.
+ *
+ * The operation is the dense product D = A x B with BF16 or FP16 inputs and
+ * FP32 accumulation ("B200 的 2CTA 怎样调优", section 七: acc = sum over k of
+ * A[i,k]*B[k,j], then the epilogue converts acc to the output type), plus the
+ * grouped expert product of "MegaMoE … 融合算子解读" (each expert's rows of A
+ * times that expert's weight matrix).
+ *
+ * Common conventions
+ *   - All matrices are row-major with element (not byte) leading dimensions:
+ *     A[i,k] at A[i*lda + k], B[k,j] at B[k*ldb + j], D[i,j] at D[i*ldd + j].
+ *   - A, B and D are DEVICE pointers on the current CUDA device.  The caller
+ *     owns every buffer; the library keeps no pointer after the call returns.
+ *   - Every base pointer must be 16-byte aligned and every leading dimension
+ *     times the element size a multiple of 16 bytes (the TMA engine's rule);
+ *     otherwise the call returns BWG_ERR_ALIGNMENT and does nothing.
+ *   - Calls are asynchronous: work is enqueued on `stream` (a cudaStream_t
+ *     passed as void*, NULL = legacy default stream) and the call never
+ *     synchronises.  The return value reports host-detectable errors and
+ *     launch failures only; faults found by the kernels while running (a
+ *     barrier wait that timed out, inconsistent group offsets) are recorded
+ *     in a per-process device error word read by bwg_last_device_error().
+ *   - There is no CPU fallback: without a usable sm_103a device the calls
+ *     return BWG_ERR_CUDA or BWG_ERR_UNSUPPORTED.
+ *   - Thread safety: calls may come from several host threads; the internal
+ *     tensor-descriptor cache is guarded by a mutex.
+ */
+#ifndef BWGEMM_H
+#define BWGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BWG_OK = 0,
+  BWG_ERR_INVALID_ARG = 1, /* null pointer, negative size, ld too small, bad dtype */
+  BWG_ERR_ALIGNMENT = 2,   /* pointer or leading dimension breaks the 16-byte rule */
+  BWG_ERR_UNSUPPORTED = 3, /* device is not sm_103 / sm_100 family, or size beyond limits */
+  BWG_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
+  BWG_ERR_TIMEOUT = 5      /* a kernel gave up waiting on a barrier (device error word) */
+} bwg_status;
+
+typedef enum { BWG_OUT_BF16 = 0, BWG_OUT_FP32 = 1, BWG_OUT_FP16 = 2 } bwg_out_dtype;
+
+/*
+ * D[M,N] = A[M,K] x B[K,N]; A and B BF16; FP32 accumulation; D in out_dtype.
+ * "使用 Warp Specialization 和 Cluster 扩展 GEMM" (steps 7-8) describes the
+ * kernel family: TMA producer, tcgen05 MMA issuer and epilogue warps over an
+ * mbarrier ring, 256x256 tiles on CTA pairs.  M <= 128 takes the swapped
+ * narrow-N kernel of "MegaMoE …" section 04.
+ *   lda >= K, ldb >= N, ldd >= N.  M, N or K == 0: M or N == 0 is a no-op;
+ *   K == 0 writes D = 0.  Sizes above 2^31-1 elements per dimension are not
+ *   supported.  Returns BWG_OK once the work is enqueued.
+ */
+bwg_status gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K, int lda, int ldb,
+                     int ldd, int out_dtype, void* stream);
+
+/* Same as gemm_bf16 with FP16 inputs. */
+bwg_status gemm_fp16(const void* A, const void* B, void* D, int M, int N, int K, int lda, int ldb,
+                     int ldd, int out_dtype, void* stream);
+
+/*
+ * Grouped expert product ("MegaMoE … 融合算子解读", expert GEMMs over routed
+ * token buckets): for g in [0, G), rows group_offsets[g] .. group_offsets[g+1]-1
+ *     D[r, :] = A[r, :] x B[g]     (r in that range)
+ *   A: device [M_total, K] BF16, dense (lda = K).
+ *   B: HOST array of G device pointers, each [K, N] BF16 row-major (ldb = N).
+ *   D: device [M_total, N] BF16, dense (ldd = N).
+ *   group_offsets: DEVICE int32 [G+1], group_offsets[0] = 0, non-decreasing,
+ *     group_offsets[G] = M_total; empty groups are allowed.  The values are
+ *     read by the kernel (no host synchronisation); offsets that break this
+ *     contract are clamped into [0, M_total] and reported through the device
+ *     error word (kind 2).
+ *   M_total is the row count of A and D: the host needs it for the tensor
+ *   descriptors because the offsets live on the device.
+ *   G may exceed 64; groups are then processed in launches of 64.
+ */
+bwg_status grouped_gemm_bf16(const void* A, const void* const* B, void* D, const int* group_offsets,
+                             int G, int M_total, int N, int K, void* stream);
+
+/* Same as grouped_gemm_bf16 with FP16 inputs and FP16 output. */
+bwg_status grouped_gemm_fp16(const void* A, const void* const* B, void* D, const int* group_offsets,
+                             int G, int M_total, int N, int K, void* stream);
+
+/*
+ * End-to-end convenience form of gemm_bf16 for host-resident data: copies
+ * A_host [M,K] and B_host [K,N] (dense, BF16, preferably pinned) into the
+ * caller's device buffers dA, dB, runs the product into dD ([M,N], out_dtype)
+ * and copies dD back to D_host, all enqueued on `stream` in that order.  The
+ * library allocates nothing; the caller synchronises the stream before
+ * reading D_host.
+ */
+bwg_status gemm_bf16_host(const void* A_host, const void* B_host, void* D_host, int M, int N, int K,
+                          int out_dtype, void* dA, void* dB, void* dD, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* bwg_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the
+ * current device.  *info receives the raw word (0 if no fault):
+ *   bits 56..63 kind (1 barrier wait timed out, 2 invalid group offsets),
+ *   48..55 role (0 TMA producer, 1 MMA issuer, 2 epilogue),
+ *   40..47 barrier (0 stage full, 1 stage empty, 2 accumulator full,
+ *   3 accumulator empty), 16..39 block index, 8..15 stage, 0..7 phase.
+ * Returns BWG_OK, BWG_ERR_TIMEOUT (kind 1), BWG_ERR_INVALID_ARG (kind 2) or
+ * BWG_ERR_CUDA.  After a timeout the output of the faulting call is undefined.
+ */
+bwg_status bwg_last_device_error(void* stream, unsigned long long* info);
+
+/*
+ * Per-process bound on every barrier wait inside the kernels, in
+ * nanoseconds (default 2e9).  A wait that exceeds it records a fault and the
+ * kernel unwinds instead of hanging.
+ */
+void bwg_set_watchdog_ns(unsigned long long ns);
+
+/*
+ * Test hook: adds `bytes` to the transaction count every stage expects, so
+ * the stage barriers can never complete and the watchdog path runs.  0 (the
+ * default) in normal use.
+ */
+void bwg_debug_set_tx_extra(unsigned int bytes);
+
+/* ---------------------------------------------------------------------
+ * Host-only planning and layout helpers (no GPU needed; used by tests).
+ * ------------------------------------------------------------------- */
+
+typedef enum {
+  BWG_KERNEL_NONE = 0,     /* nothing to launch (empty problem) */
+  BWG_KERNEL_ZERO = 1,     /* K == 0: D = 0 */
+  BWG_KERNEL_1CTA = 2,     /* 128 x 256 tiles, one CTA each */
+  BWG_KERNEL_2CTA = 3,     /* 256 x 256 tiles on CTA pairs (cta_group::2) */
+  BWG_KERNEL_SMALL_M = 4   /* swapped operands, MMA N = M rounded up to 16 */
+} bwg_kernel_kind;
+
+typedef struct {
+  int kernel;              /* bwg_kernel_kind */
+  int tile_m, tile_n, tile_k;
+  int mma_m, mma_n;        /* shape of one tcgen05.mma (mma_n = padded M for SMALL_M) */
+  int stages;              /* SMEM ring depth */
+  int tiles;               /* output tiles */
+  int k_blocks;            /* ceil(K / tile_k) */
+  double coverage;         /* M*N / (tiles * tile_m * tile_n) */
+  int smem_input_per_cta;  /* bytes of A+B ring per CTA (stages x stage bytes) */
+  int smem_total;          /* dynamic shared memory requested per CTA */
+  int grid;                /* CTAs launched for `sm_count` SMs */
+  uint32_t tx_bytes;       /* bytes the stage barrier expects per k-block */
+  uint32_t idesc;          /* instruction descriptor */
+} bwg_plan_info;
+
+/*
+ * Plans a dense call without touching the GPU.  force_kernel = 0 lets the
+ * planner choose; force_stages = 0 picks the deepest ring that fits in
+ * shared memory.  sm_count sizes the persistent grid.
+ */
+bwg_status bwg_plan(int M, int N, int K, int out_dtype, int sm_count, int force_kernel,
+                    int force_stages, bwg_plan_info* out);
+
+/* Argument validation exactly as gemm_bf16/gemm_fp16 apply it (host only). */
+bwg_status bwg_check_gemm_args(const void* A, const void* B, const void* D, int M, int N, int K,
+                               int lda, int ldb, int ldd, int out_dtype);
+
+/* tcgen05 instruction descriptor, kind::f16 with FP32 accumulation
+ * (bf16 != 0: BF16 inputs, else FP16; *_mn_major != 0: operand MN-major). */
+uint32_t bwg_idesc_f16(int bf16, int a_mn_major, int b_mn_major, int m, int n);
+
+/* tcgen05 shared-memory matrix descriptor (swizzle: 0 none, 2 = 128-byte). */
+uint64_t bwg_smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes, int swizzle);
+
+/* Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled tile. */
+uint32_t bwg_swizzle128_offset(uint32_t row, uint32_t chunk);
+
+/* Output tile (m_tile, n_tile) processed at linear position t of the
+ * grouped raster order used by the dense kernels (host copy of the device
+ * scheduler, for tests). */
+void bwg_raster_tile(int t, int num_m_tiles, int num_n_tiles, int group_m, int* m_tile,
+                     int* n_tile);
+
+/* Host copy of the grouped schedule the grouped kernels run (for tests).
+ * offsets: HOST int32 [G+1].  Fills prefix[G+1] (tiles before each group),
+ * lo[G], hi[G] (clamped row ranges) for tiles of tile_m rows and 256 columns
+ * over N columns; returns 1 if the offsets honour the contract, else 0. */
+int bwg_grouped_schedule(const int* offsets, int G, int M_total, int N, int tile_m, int* prefix,
+                         int* lo, int* hi);
+
+/* Tile t of that schedule: group, first row, first column, row end. */
+void bwg_grouped_tile(int t, int G, const int* prefix, const int* lo, const int* hi, int tile_m,
+                      int* g, int* m0, int* n0, int* row_end);
+
+/* Library version string. */
+const char* bwg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BWGEMM_H */

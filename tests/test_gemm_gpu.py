@@ -1,0 +1,189 @@
+"""GPU parity of the dense kernels against the CPU oracle (through the C ABI).
+
+Acceptance: bit-exact where the inputs are integers and every partial sum is
+exact in binary32; otherwise |D - D_ref| <= 2^-7 |D_ref| + 1e-3 S elementwise
+(S = sum_k |a_ik b_kj|), the bound the method states, for every output type."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from blackwell_tensor_core_gb300 import workloads as wl
+from gpu_util import assert_bits_equal, assert_within_bound, gpu_gemm, in_dtype_name
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from blackwell_tensor_core_gb300 import build
+    build.build()
+
+
+# ---------------------------------------------------------------- exact ----
+
+@pytest.mark.parametrize("kind", ["2cta", "1cta"])
+def test_tile_case_exact(kind):
+    """256x256x512 integers in {-2..2}, FP32 out: every partial sum is an
+    integer below 2^24, so the result is exact in any summation order."""
+    c = wl.tile_case()
+    D, _ = gpu_gemm(c.A, c.B, wl.OUT_FP32, kind)
+    Dref, _ = oracle.gemm(wl.bits(c.A), wl.bits(c.B))
+    assert np.array_equal(D.double().numpy(), Dref)
+
+
+@pytest.mark.parametrize("kind", ["2cta", "1cta"])
+@pytest.mark.parametrize("out", [wl.OUT_BF16, wl.OUT_FP16])
+def test_integer_inputs_rounded_output_exact(kind, out):
+    g = wl.generator(2001)
+    A = wl.randint_matrix(384, 1024, -2, 2, g)
+    B = wl.randint_matrix(1024, 520, -2, 2, g)
+    D, _ = gpu_gemm(A, B, out, kind)
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+    assert_bits_equal(D, oracle.round_to(Dref, "fp16" if out == wl.OUT_FP16 else "bf16"), kind)
+
+
+@pytest.mark.parametrize("M", [1, 16, 72, 100, 128])
+def test_small_m_integer_exact(M):
+    g = wl.generator(2002 + M)
+    A = wl.randint_matrix(M, 640, -2, 2, g)
+    B = wl.randint_matrix(640, 1000, -2, 2, g)
+    D, _ = gpu_gemm(A, B, wl.OUT_FP32, None)
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+    assert np.array_equal(D.double().numpy(), Dref)
+    D16, _ = gpu_gemm(A, B, wl.OUT_BF16, None)
+    assert_bits_equal(D16, oracle.round_to(Dref, "bf16"), "small_m bf16")
+
+
+# ------------------------------------------------------- bound, ragged -----
+
+SHAPES = [(520, 600, 456), (300, 264, 72), (129, 8, 8), (256, 256, 64), (1000, 136, 1000),
+          (257, 520, 40), (768, 1024, 2048)]
+
+
+@pytest.mark.parametrize("kind", ["2cta", "1cta"])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_random_shapes_within_bound(kind, shape):
+    M, N, K = shape
+    g = wl.generator(3000 + M + N + K)
+    A = wl.normal_matrix(M, K, 1.0, g)
+    B = wl.normal_matrix(K, N, 1.0, g)
+    Dref, S = oracle.gemm(wl.bits(A), wl.bits(B))
+    for out in (wl.OUT_BF16, wl.OUT_FP32):
+        D, _ = gpu_gemm(A, B, out, kind)
+        assert_within_bound(D, Dref, S, "%s %s out=%d" % (kind, shape, out))
+
+
+@pytest.mark.parametrize("shape", [(1, 8, 8), (17, 200, 104), (72, 1000, 520), (128, 384, 64),
+                                   (16, 16, 16), (33, 4104, 1000)])
+@pytest.mark.parametrize("out", [wl.OUT_BF16, wl.OUT_FP32, wl.OUT_FP16])
+def test_small_m_within_bound(shape, out):
+    M, N, K = shape
+    g = wl.generator(4000 + M + N + K)
+    A = wl.normal_matrix(M, K, 1.0, g)
+    B = wl.normal_matrix(K, N, 1.0, g)
+    Dref, S = oracle.gemm(wl.bits(A), wl.bits(B))
+    D, _ = gpu_gemm(A, B, out, None)
+    assert_within_bound(D, Dref, S, "small_m %s out=%d" % (shape, out))
+
+
+@pytest.mark.parametrize("kind", ["2cta", "1cta", None])
+def test_fp16_inputs(kind):
+    M = 72 if kind is None else 400
+    g = wl.generator(5000)
+    A = wl.normal_matrix(M, 328, 1.0, g, "fp16")
+    B = wl.normal_matrix(328, 392, 1.0, g, "fp16")
+    Dref, S = oracle.gemm(wl.bits(A), wl.bits(B), "fp16")
+    for out in (wl.OUT_FP16, wl.OUT_FP32, wl.OUT_BF16):
+        D, _ = gpu_gemm(A, B, out, kind)
+        assert_within_bound(D, Dref, S, "fp16 in %s out=%d" % (kind, out))
+
+
+@pytest.mark.parametrize("kind", ["2cta", "1cta", None])
+def test_leading_dimensions_and_untouched_padding(kind):
+    M = 90 if kind is None else 300
+    N, K = 200, 136
+    g = wl.generator(5100)
+    A = wl.normal_matrix(M, K, 1.0, g)
+    B = wl.normal_matrix(K, N, 1.0, g)
+    Dref, S = oracle.gemm(wl.bits(A), wl.bits(B))
+    D, full = gpu_gemm(A, B, wl.OUT_BF16, kind, lda=K + 24, ldb=N + 56, ldd=N + 40, sentinel=7.0)
+    assert_within_bound(D, Dref, S, "strided %s" % kind)
+    assert torch.all(full[:, N:] == 7.0), "padding columns of D were written"
+
+
+def test_k_zero_writes_zeros_and_empty_is_noop():
+    from blackwell_tensor_core_gb300 import ops
+    D = torch.full((37, 64), 5.0, dtype=torch.bfloat16, device="cuda")
+    ops.gemm_bf16(0, 0, D.data_ptr(), 37, 64, 0, 0, 0, 64, 0, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert torch.all(D == 0)
+    ops.gemm_bf16(0, 0, 0, 0, 64, 10, 0, 0, 0, 0, torch.cuda.current_stream().cuda_stream)
+
+
+def test_short_k_below_one_block():
+    for K in (8, 16, 24, 56):
+        g = wl.generator(5200 + K)
+        A = wl.randint_matrix(300, K, -2, 2, g)
+        B = wl.randint_matrix(K, 264, -2, 2, g)
+        D, _ = gpu_gemm(A, B, wl.OUT_FP32, None)
+        Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+        assert np.array_equal(D.double().numpy(), Dref)
+
+
+def test_bad_arguments_return_status():
+    from blackwell_tensor_core_gb300 import ops
+    D = torch.empty((64, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ops.BwgError) as e:
+        ops.gemm_bf16(D.data_ptr() + 2, D.data_ptr(), D.data_ptr(), 64, 64, 64, 64, 64, 64, 0, 0)
+    assert e.value.status == 2
+
+
+# ------------------------------------------- full-size method workloads ----
+
+def _sample_indices(M, N, n, seed, tile_m=256, tile_n=256):
+    rng = np.random.default_rng(seed)
+    I = list(rng.integers(0, M, n))
+    J = list(rng.integers(0, N, n))
+    # tile corners and edges
+    for m in sorted({0, 127, 128, 255, tile_m, M - 1, M // 2}):
+        for nn in sorted({0, 63, 64, 127, 128, 255, tile_n, N - 1}):
+            if m < M and nn < N:
+                I.append(m)
+                J.append(nn)
+    return np.array(I), np.array(J)
+
+
+def _check_sampled(A, B, D, n, seed, what):
+    M, N = D.shape
+    I, J = _sample_indices(M, N, n, seed)
+    Dref, S = oracle.gemm_elements(wl.bits(A), wl.bits(B), I, J, in_dtype_name(A))
+    assert_within_bound(D[I, J], Dref, S, what)
+    return I, J
+
+
+def test_square_4096_sampled():
+    c = wl.square_case()
+    D, _ = gpu_gemm(c.A, c.B, c.out_dtype)
+    assert torch.isfinite(D.float()).all()
+    _check_sampled(c.A, c.B, D, 20000, 11, c.name)
+
+
+def test_large_8192_sampled_in_bench_configuration():
+    c = wl.large_case()
+    D, _ = gpu_gemm(c.A, c.B, c.out_dtype)
+    assert torch.isfinite(D.float()).all()
+    _check_sampled(c.A, c.B, D, 20000, 12, c.name)
+    # whole rows and columns at tile seams
+    for r in (0, 255, 256, 8191):
+        Dref, S = oracle.gemm(wl.bits(c.A[r:r + 1]), wl.bits(c.B))
+        assert_within_bound(D[r:r + 1], Dref, S, "row %d" % r)
+
+
+def test_small_m_method_workload_full():
+    c = wl.small_m_case()
+    D, _ = gpu_gemm(c.A, c.B, c.out_dtype)
+    Dref, S = oracle.gemm(wl.bits(c.A), wl.bits(c.B))
+    assert_within_bound(D, Dref, S, c.name)

@@ -1,0 +1,103 @@
+"""GPU parity of the grouped (expert FC1) kernel against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from blackwell_tensor_core_gb300 import workloads as wl
+from gpu_util import assert_bits_equal, assert_within_bound
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from blackwell_tensor_core_gb300 import build
+    build.build()
+
+
+def run_grouped(A, Bs, offsets, sentinel=float("nan")):
+    from blackwell_tensor_core_gb300 import ops
+    dev = torch.device("cuda")
+    Ad = A.to(dev)
+    Bd = [b.to(dev) for b in Bs]
+    off = torch.from_numpy(np.asarray(offsets, dtype=np.int32)).to(dev)
+    N = Bs[0].shape[1]
+    D = torch.full((A.shape[0], N), sentinel, dtype=A.dtype, device=dev)
+    ops.grouped_gemm(Ad, Bd, off, out=D)
+    torch.cuda.synchronize()
+    st, word = ops.last_device_error()
+    return D.cpu(), st, word
+
+
+def test_grouped_integer_exact_with_empty_and_ragged_groups():
+    counts = [300, 0, 256, 1, 0, 511, 37]
+    off = wl.offsets_from_counts(counts)
+    g = wl.generator(6000)
+    K, N = 200, 600
+    A = wl.randint_matrix(int(off[-1]), K, -2, 2, g)
+    Bs = [wl.randint_matrix(K, N, -2, 2, g) for _ in counts]
+    D, st, word = run_grouped(A, Bs, off)
+    assert st == 0, hex(word)
+    Dref, _ = oracle.grouped_gemm(wl.bits(A), [wl.bits(b) for b in Bs], off)
+    assert_bits_equal(D, oracle.round_to(Dref, "bf16"), "grouped exact")
+
+
+def test_grouped_random_within_bound_single_group_and_fp16():
+    g = wl.generator(6001)
+    for dtype in ("bf16", "fp16"):
+        A = wl.normal_matrix(700, 264, 1.0, g, dtype)
+        Bs = [wl.normal_matrix(264, 520, 0.5, g, dtype)]
+        off = np.array([0, 700], np.int32)
+        D, st, word = run_grouped(A, Bs, off)
+        assert st == 0, hex(word)
+        Dref, S = oracle.grouped_gemm(wl.bits(A), [wl.bits(b) for b in Bs], off, dtype)
+        assert_within_bound(D, Dref, S, "grouped G=1 " + dtype)
+
+
+def test_grouped_more_than_64_groups():
+    rng = np.random.default_rng(6002)
+    counts = list(rng.integers(0, 40, 70))
+    off = wl.offsets_from_counts(counts)
+    g = wl.generator(6003)
+    K, N = 64, 256
+    A = wl.randint_matrix(int(off[-1]), K, -2, 2, g)
+    Bs = [wl.randint_matrix(K, N, -2, 2, g) for _ in counts]
+    D, st, word = run_grouped(A, Bs, off)
+    assert st == 0, hex(word)
+    Dref, _ = oracle.grouped_gemm(wl.bits(A), [wl.bits(b) for b in Bs], off)
+    assert_bits_equal(D, oracle.round_to(Dref, "bf16"), "grouped G=70")
+
+
+def test_grouped_bad_offsets_are_reported_and_stay_in_bounds():
+    g = wl.generator(6004)
+    A = wl.normal_matrix(300, 64, 1.0, g)
+    Bs = [wl.normal_matrix(64, 256, 1.0, g) for _ in range(3)]
+    off = np.array([0, 200, 100, 300], np.int32)  # decreasing: breaks the contract
+    D, st, word = run_grouped(A, Bs, off, sentinel=3.0)
+    assert st == 1 and (word >> 56) == 2
+    # clamped schedule: group 1 is empty, groups 0 and 2 still computed
+    Dref0, S0 = oracle.gemm(wl.bits(A[:200]), wl.bits(Bs[0]))
+    assert_within_bound(D[:200], Dref0, S0, "group 0")
+
+
+def test_grouped_fc1_method_workload_sampled():
+    c = wl.grouped_case()
+    D, st, word = run_grouped(c.A, c.Bs, c.offsets)
+    assert st == 0, hex(word)
+    assert torch.isfinite(D.float()).all()
+    rng = np.random.default_rng(13)
+    Abits = wl.bits(c.A)
+    for gi in range(c.G):
+        r0, r1 = int(c.offsets[gi]), int(c.offsets[gi + 1])
+        if r1 == r0:
+            continue
+        rows = np.concatenate([[r0, r1 - 1, min(r0 + 255, r1 - 1), min(r0 + 256, r1 - 1)],
+                               rng.integers(r0, r1, 60)])
+        cols = np.concatenate([[0, 4095, 255, 256, 2047], rng.integers(0, c.N, 59)])
+        I = np.repeat(rows, 1)
+        J = cols[: len(rows)]
+        Dref, S = oracle.gemm_elements(Abits, wl.bits(c.Bs[gi]), I, J)
+        assert_within_bound(D[I, J], Dref, S, "expert %d" % gi)

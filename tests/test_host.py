@@ -1,0 +1,209 @@
+"""Host-side tests of the C library (no GPU): exported symbols, argument
+checks, planner values against figures printed on the pages, descriptor
+encoders against words derived by hand from the PTX ISA field tables, the
+128-byte swizzle, and the tile schedules."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden", "page_budgets.txt")
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from blackwell_tensor_core_gb300 import build as b
+    b.build()
+    from blackwell_tensor_core_gb300 import ops as o
+    return o
+
+
+def _golden():
+    rows = {}
+    for line in open(GOLDEN, encoding="utf-8"):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, *vals = line.split()
+        rows.setdefault(key, []).append([float(v) for v in vals])
+    return rows
+
+
+def test_library_exports_every_declared_function(ops):
+    header = open(os.path.join(ROOT, "include", "bwgemm.h"), encoding="utf-8").read()
+    header = re.sub(r"/\*.*?\*/", "", header, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w ]*?[\s\*]+(\w+)\s*\(", header, flags=re.M)
+    names = [n for n in names if n not in ("if", "return")]
+    assert {"gemm_bf16", "gemm_fp16", "grouped_gemm_bf16", "bwg_last_device_error"} <= set(names)
+    raw = ctypes.CDLL(ops.LIB_PATH)
+    missing = [n for n in names if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_status_strings(ops):
+    assert ops.status_string(0) == "ok"
+    assert "align" in ops.status_string(2)
+    assert ops.lib().bwg_version().decode().startswith("bwgemm")
+
+
+def test_argument_checks(ops):
+    ok, inv, ali = 0, 1, 2
+    A, B, D = 0x10000, 0x20000, 0x30000
+    c = ops.check_gemm_args
+    assert c(A, B, D, 256, 256, 512, 512, 256, 256, 0) == ok
+    assert c(A, B, D, 256, 256, 512, 512, 256, 256, 7) == inv          # bad out dtype
+    assert c(A, B, D, -1, 256, 512, 512, 256, 256, 0) == inv
+    assert c(0, B, D, 256, 256, 512, 512, 256, 256, 0) == inv          # null A
+    assert c(A, B, 0, 256, 256, 512, 512, 256, 256, 0) == inv          # null D
+    assert c(A, B, D, 256, 256, 512, 500, 256, 256, 0) == inv          # lda < K
+    assert c(A, B, D, 256, 256, 512, 512, 200, 256, 0) == inv          # ldb < N
+    assert c(A, B, D, 256, 256, 512, 512, 256, 100, 0) == inv          # ldd < N
+    assert c(A + 8, B, D, 256, 256, 512, 512, 256, 256, 0) == ali      # misaligned A
+    assert c(A, B, D, 256, 256, 512, 516, 256, 256, 0) == ali          # lda*2 not 16-byte
+    assert c(A, B, D, 256, 260, 512, 512, 260, 264, 0) == ali          # ldb*2 = 520
+    assert c(A, B, D, 256, 260, 512, 512, 264, 260, 1) == ok           # fp32 D: 260*4 = 1040
+    assert c(A, B, D, 256, 260, 512, 512, 264, 260, 0) == ali          # bf16 D: 520
+    assert c(0, 0, 0, 0, 256, 512, 0, 0, 0, 0) == ok                   # empty problem
+    assert c(0, 0, D, 4, 8, 0, 0, 0, 8, 0) == ok                       # K = 0: only D needed
+
+
+def test_planner_matches_page_calculator(ops):
+    g = _golden()
+    M, N, K, stages, tiles, cov, kib, kblocks = g["calculator"][0]
+    p = ops.plan(int(M), int(N), int(K), force_kernel=ops.KERNEL_2CTA, force_stages=int(stages))
+    assert (p.tile_m, p.tile_n, p.tile_k) == (256, 256, 64)
+    assert p.tiles == tiles
+    assert round(p.coverage * 100, 1) == cov
+    assert p.smem_input_per_cta // 1024 == kib
+    assert p.k_blocks == kblocks
+
+
+def test_planner_stage_and_barrier_accounting(ops):
+    g = _golden()
+    lone, pair = g["per_cta_kib"][0]
+    p1 = ops.plan(512, 512, 512, force_kernel=ops.KERNEL_1CTA, force_stages=2)
+    p2 = ops.plan(512, 512, 512, force_kernel=ops.KERNEL_2CTA, force_stages=2)
+    assert p1.smem_input_per_cta // 2 // 1024 == lone
+    assert p2.smem_input_per_cta // 2 // 1024 == pair
+    assert 2 * 256 * 256 * 64 == g["round_flops"][0][0]
+    assert p2.smem_input_per_cta // 2 // 1024 == g["stage_kib"][0][0]
+    staging_kib = 32  # four epilogue warps x two 4 KiB boxes
+    for depth, total in g["depth_total_kib"]:
+        p = ops.plan(4096, 4096, 4096, force_kernel=ops.KERNEL_2CTA, force_stages=int(depth))
+        assert p.smem_input_per_cta // 1024 + staging_kib == total
+        assert p.smem_total <= 232448
+    assert p2.tx_bytes == g["tx_bytes"][0][0]
+    assert 128 * 256 * 4 // 1024 == g["accumulator_kib"][0][0]
+
+
+def test_planner_choices(ops):
+    big = ops.plan(8192, 8192, 8192)
+    assert big.kernel == ops.KERNEL_2CTA and big.stages == 6 and big.tiles == 1024
+    assert big.grid == 152 and big.smem_total <= 232448
+    small = ops.plan(72, 16384, 7168)
+    assert small.kernel == ops.KERNEL_SMALL_M and small.mma_n == 80 and small.tiles == 128
+    assert small.smem_total <= 232448 and small.stages >= 4
+    for tokens, n in _golden()["n_compute"]:
+        assert ops.plan(int(tokens), 4096, 4096).mma_n == n
+    assert ops.plan(0, 10, 10).kernel == ops.KERNEL_NONE
+    assert ops.plan(10, 10, 0).kernel == ops.KERNEL_ZERO
+    assert ops.plan(129, 10, 10).kernel == ops.KERNEL_2CTA
+    assert ops.plan(128, 10, 10).kernel == ops.KERNEL_SMALL_M
+
+
+def test_instruction_descriptor_words(ops):
+    # Fields (PTX ISA, tcgen05 instruction descriptor for kind::f16):
+    # bit 4 = D is F32, bits 7-9 A format (1 = BF16), bits 10-12 B format,
+    # bit 15/16 A/B MN-major, bits 17-22 N>>3, bits 24-28 M>>4.
+    # Pair tile, BF16, A K-major, B MN-major, M = N = 256:
+    want = (1 << 4) | (1 << 7) | (1 << 10) | (1 << 16) | ((256 >> 3) << 17) | ((256 >> 4) << 24)
+    assert want == 0x10410490
+    assert ops.lib().bwg_idesc_f16(1, 0, 1, 256, 256) == want
+    # swapped small-M kernel, FP16, A MN-major, B K-major, M = 128, N = 80
+    want = (1 << 4) | (1 << 15) | ((80 >> 3) << 17) | ((128 >> 4) << 24)
+    assert ops.lib().bwg_idesc_f16(0, 1, 0, 128, 80) == want
+    # the N field alone, as the MegaMoE page prints it: (N >> 3) << 17
+    for n in range(16, 257, 16):
+        w = ops.lib().bwg_idesc_f16(1, 0, 0, 128, n)
+        assert (w >> 17) & 0x3F == n >> 3
+        assert w & ~(0x3F << 17) == ops.lib().bwg_idesc_f16(1, 0, 0, 128, 16) & ~(0x3F << 17)
+
+
+def test_shared_memory_descriptor_words(ops):
+    # start >> 4 in bits 0-13, LBO >> 4 in 16-29, SBO >> 4 in 32-45,
+    # version 1 at bit 46, swizzle mode in 61-63 (2 = 128-byte).
+    d = ops.lib().bwg_smem_desc(0x1400, 8192, 1024, 2)
+    assert d == (0x140) | (512 << 16) | (64 << 32) | (1 << 46) | (2 << 61)
+    d = ops.lib().bwg_smem_desc(0x3FFF0, 16, 1024, 2)
+    assert d & 0x3FFF == 0x3FFF
+    assert (d >> 16) & 0x3FFF == 1
+
+
+def test_swizzle_matches_page_formula_and_is_a_permutation(ops):
+    f = ops.lib().bwg_swizzle128_offset
+    for row in range(64):
+        offs = [f(row, c) for c in range(8)]
+        # "GEMM优化（三）" 2.1: physical = row*128 + ((chunk ^ (row % 8)) * 16)
+        assert offs == [row * 128 + ((c ^ (row % 8)) * 16) for c in range(8)]
+        assert sorted(offs) == [row * 128 + 16 * c for c in range(8)]
+    # the eight rows of one atom put a given chunk in eight different bank groups
+    for c in range(8):
+        assert len({(f(r, c) % 128) // 16 for r in range(8)}) == 8
+
+
+@pytest.mark.parametrize("mt,nt,gm", [(32, 32, 8), (16, 16, 8), (5, 7, 8), (9, 3, 4), (1, 1, 8), (13, 11, 16)])
+def test_raster_order_covers_every_tile_once(ops, mt, nt, gm):
+    m = ctypes.c_int()
+    n = ctypes.c_int()
+    seen = set()
+    for t in range(mt * nt):
+        ops.lib().bwg_raster_tile(t, mt, nt, gm, ctypes.byref(m), ctypes.byref(n))
+        assert 0 <= m.value < mt and 0 <= n.value < nt
+        seen.add((m.value, n.value))
+        # inside one raster group the row index stays within the group's rows
+        assert m.value // gm == t // (gm * nt)
+    assert len(seen) == mt * nt
+
+
+def _schedule(ops, offsets, N, tile_m):
+    G = len(offsets) - 1
+    ia = ctypes.c_int * (G + 1)
+    off = ia(*offsets)
+    prefix, lo, hi = ia(), ia(), ia()
+    ok = ops.lib().bwg_grouped_schedule(off, G, offsets[-1], N, tile_m, prefix, lo, hi)
+    return ok, list(prefix), list(lo)[:G], list(hi)[:G]
+
+
+def test_grouped_schedule_covers_every_row_and_column_once(ops):
+    counts = [300, 0, 256, 1, 0, 511, 1024, 0]
+    offsets = [0] + list(np.cumsum(counts))
+    N, tile_m = 600, 256
+    ok, prefix, lo, hi = _schedule(ops, offsets, N, tile_m)
+    assert ok == 1
+    n_tiles = (N + 255) // 256
+    want = [((c + tile_m - 1) // tile_m) * n_tiles for c in counts]
+    assert prefix == list(np.concatenate([[0], np.cumsum(want)]))
+    G = len(counts)
+    covered = np.zeros((offsets[-1], n_tiles), dtype=int)
+    g, m0, n0, re_ = (ctypes.c_int() for _ in range(4))
+    P = (ctypes.c_int * (G + 1))(*prefix)
+    L = (ctypes.c_int * G)(*lo)
+    H = (ctypes.c_int * G)(*hi)
+    for t in range(prefix[-1]):
+        ops.lib().bwg_grouped_tile(t, G, P, L, H, tile_m, ctypes.byref(g), ctypes.byref(m0),
+                                   ctypes.byref(n0), ctypes.byref(re_))
+        assert counts[g.value] > 0
+        assert offsets[g.value] <= m0.value < offsets[g.value + 1] == re_.value
+        rows = range(m0.value, min(m0.value + tile_m, re_.value))
+        covered[list(rows), n0.value // 256] += 1
+    assert (covered == 1).all()
+
+
+def test_grouped_schedule_flags_bad_offsets(ops):
+    assert _schedule(ops, [0, 10, 5, 20], 256, 256)[0] == 0      # decreasing
+    assert _schedule(ops, [3, 10, 20], 256, 256)[0] == 0         # first != 0
+    ok, prefix, lo, hi = _schedule(ops, [0, 10, 5, 20], 256, 256)
+    assert all(l <= h for l, h in zip(lo, hi)) and lo[1] >= hi[0]  # clamped, disjoint
