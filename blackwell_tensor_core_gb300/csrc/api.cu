@@ -99,6 +99,11 @@ int small_m_smem(int m_pad, int out_dtype, int stages) {
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
+int no_tail_split_from_env() {
+  const char* v = std::getenv("BWG_NO_TAIL_SPLIT");
+  return (v != nullptr && v[0] == '1') ? 1 : 0;
+}
+
 bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_count, int max_smem,
                       int force_kernel, int force_stages, int max_clusters_2cta, int max_ctas_1cta,
                       bwg_plan_info* o) {
@@ -159,6 +164,11 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     o->idesc = make_idesc_f16(fmt, /*a_mn_major=*/false, /*b_mn_major=*/true, o->mma_m, kTileN);
   }
   o->coverage = static_cast<double>(M) * N / (static_cast<double>(o->tiles) * o->tile_m * o->tile_n);
+  o->units = o->tiles;
+  if (kind != BWG_KERNEL_SMALL_M && !no_tail_split_from_env()) {
+    const int workers = kind == BWG_KERNEL_2CTA ? o->grid / 2 : o->grid;
+    o->units = o->tiles + tail_split_count(o->tiles, workers);
+  }
   return BWG_OK;
 }
 
@@ -377,6 +387,7 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
   p.out_dtype = out_dtype;
   p.idesc = pl.idesc;
   p.tx_extra = g_tx_extra.load();
+  p.no_tail_split = no_tail_split_from_env();
   if (pl.kernel == BWG_KERNEL_2CTA)
     return launch_status(launch_gemm_2cta(p, pl.grid, pl.smem_total, stream));
   return launch_status(launch_gemm_1cta(p, pl.grid, pl.smem_total, stream));
@@ -439,6 +450,7 @@ bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
     p.G = gn;
     p.g_begin = g0;
     p.G_total = G;
+    p.no_tail_split = no_tail_split_from_env();
     // Upper bound on tiles: every group adds at most one partial row tile.
     const long long max_tiles =
         (static_cast<long long>(ceil_div(M_total, 2 * kRowsPerCta)) + gn) * p.num_n_tiles;
@@ -572,6 +584,12 @@ int bwg_grouped_schedule(const int* offsets, int G, int M_total, int N, int tile
 void bwg_grouped_tile(int t, int G, const int* prefix, const int* lo, const int* hi, int tile_m,
                       int* g, int* m0, int* n0, int* row_end) {
   grouped_tile(t, G, prefix, lo, hi, tile_m, kTileN, g, m0, n0, row_end);
+}
+
+int bwg_tail_split(int T, int C) { return tail_split_count(T, C); }
+
+void bwg_unit_tile(int u, int T, int R, int tile_n, int* tile, int* col_off, int* width) {
+  unit_tile(u, T, R, tile_n, tile, col_off, width);
 }
 
 const char* bwg_version(void) { return "bwgemm 0.1 (sm_103a)"; }

@@ -49,11 +49,13 @@ __device__ __forceinline__ void record_fault(unsigned long long* err, unsigned l
   atomicCAS(err, 0ull, code);
 }
 
-// One output tile of the cluster: first row (of the pair), first column, the
-// row bound for stores (M, or the end of the tile's group) and the group.
+// One work unit of the cluster: first row (of the pair), first column, its
+// width in columns (a whole tile, or half of one in the last wave), the row
+// bound for stores (M, or the end of the unit's group) and the group.
 struct Tile {
   int m0;
   int n0;
+  int width;
   int row_end;
   int g;
 };
@@ -65,16 +67,25 @@ struct Sched {
   const int* prefix;  // grouped tables in shared memory: prefix[G+1], lo[G], hi[G]
   const int* lo;
   const int* hi;
+  int tiles;          // whole tiles
+  int split;          // tiles of the last wave split in two along N
 
-  __device__ int total() const {
+  __device__ Sched(const GemmParams& p_, const int* prefix_, const int* lo_, const int* hi_,
+                   int workers)
+      : p(p_), prefix(prefix_), lo(lo_), hi(hi_) {
     if constexpr (GROUPED)
-      return prefix[p.G];
+      tiles = prefix[p.G];
     else
-      return p.num_m_tiles * p.num_n_tiles;
+      tiles = p.num_m_tiles * p.num_n_tiles;
+    split = p.no_tail_split ? 0 : tail_split_count(tiles, workers);
   }
 
-  __device__ Tile at(int t) const {
+  __device__ int total() const { return tiles + split; }
+
+  __device__ Tile at(int u) const {
     Tile tl;
+    int t, col_off;
+    unit_tile(u, tiles, split, kTileN, &t, &col_off, &tl.width);
     if constexpr (GROUPED) {
       grouped_tile(t, p.G, prefix, lo, hi, kTileM, kTileN, &tl.g, &tl.m0, &tl.n0, &tl.row_end);
     } else {
@@ -85,6 +96,7 @@ struct Sched {
       tl.row_end = p.M;
       tl.g = 0;
     }
+    tl.n0 += col_off;
     return tl;
   }
 };
@@ -112,9 +124,8 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
   const int S = p.stages;
-  constexpr uint32_t kBCols = kTileN / CG;             // B columns this CTA loads
+  constexpr uint32_t kBCols = kTileN / CG;             // B columns a CTA loads for a whole tile
   constexpr uint32_t kBStageBytes = kBCols * kBK * 2;  // 32 KiB (1 CTA) or 16 KiB (pair)
-  constexpr uint32_t kBChunks = kBCols / 64;
 
   const uint32_t smem_a = base;
   const uint32_t smem_b = smem_a + S * kAStageBytes;
@@ -168,10 +179,10 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
   tc_fence_after();
   const uint32_t tmem_base = ld_shared_u32(tmem_slot);
 
-  const Sched<CG, GROUPED> sched{p, t_prefix, t_lo, t_hi};
-  const int total = sched.total();
   const int first = static_cast<int>((CG == 2) ? cluster_id_x() : blockIdx.x);
   const int stride = static_cast<int>((CG == 2) ? num_clusters_x() : gridDim.x);
+  const Sched<CG, GROUPED> sched(p, t_prefix, t_lo, t_hi, stride);
+  const int total = sched.total();
   bool aborted = false;
 
   if (warp == 0) {
@@ -179,11 +190,13 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      const uint32_t stage_tx = CG * (kAStageBytes + kBStageBytes) + p.tx_extra;
       for (int t = first; t < total && !aborted; t += stride) {
         const Tile tl = sched.at(t);
+        const uint32_t b_cols = static_cast<uint32_t>(tl.width) / CG;  // this CTA's B columns
+        const uint32_t b_chunks = b_cols / 64;
+        const uint32_t stage_tx = CG * (kAStageBytes + b_cols * kBK * 2) + p.tx_extra;
         const int a_row = tl.m0 + static_cast<int>(rank) * kRowsPerCta;
-        const int b_col = tl.n0 + static_cast<int>(rank * kBCols);
+        const int b_col = tl.n0 + static_cast<int>(rank * b_cols);
         const CUtensorMap* mb = b_map<CG, GROUPED>(P, tl.g);
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, p.timeout_ns)) {
@@ -198,14 +211,12 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
             if (rank == 0) mbar_arrive_expect_tx(full_bar(s), stage_tx);
             const uint32_t fb = mapa_shared(full_bar(s), 0);
             tma_load_2d_pair(sa, &p.map_a, fb, k0, a_row);
-#pragma unroll
-            for (uint32_t j = 0; j < kBChunks; ++j)
+            for (uint32_t j = 0; j < b_chunks; ++j)
               tma_load_2d_pair(sb + j * kBChunkBytes, mb, fb, b_col + 64 * j, k0);
           } else {
             mbar_arrive_expect_tx(full_bar(s), stage_tx);
             tma_load_2d(sa, &p.map_a, full_bar(s), k0, a_row);
-#pragma unroll
-            for (uint32_t j = 0; j < kBChunks; ++j)
+            for (uint32_t j = 0; j < b_chunks; ++j)
               tma_load_2d(sb + j * kBChunkBytes, mb, full_bar(s), b_col + 64 * j, k0);
           }
           if (++s == S) {
@@ -231,6 +242,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * kTileN;
+        const uint32_t idesc = idesc_with_n(p.idesc, static_cast<uint32_t>(sched.at(t).width));
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait(full_bar(s), ph, p.timeout_ns)) {
             record_fault(p.err, kFaultTimeout, kRoleMma, kBarFull, s, ph);
@@ -245,7 +257,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
           for (uint32_t kk = 0; kk < kBK / 16; ++kk) {
             // K-major A: the next 16 K values are 32 bytes further along each
             // 128-byte row.  MN-major B: they are 16 rows (2048 bytes) further.
-            mma_f16<CG>(d_tmem, a_desc + ((kk * 32u) >> 4), b_desc + ((kk * 2048u) >> 4), p.idesc,
+            mma_f16<CG>(d_tmem, a_desc + ((kk * 32u) >> 4), b_desc + ((kk * 2048u) >> 4), idesc,
                         (kb | kk) != 0 ? 1u : 0u);
           }
           if constexpr (CG == 2)
@@ -290,7 +302,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
       const int row_w = tl.m0 + static_cast<int>(rank * kRowsPerCta + q * 32u);
       const uint32_t t_acc = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc) * kTileN;
       const int sub_cols = out32 ? 32 : 64;
-      const int nsub = kTileN / sub_cols;
+      const int nsub = tl.width / sub_cols;
       for (int sub = 0; sub < nsub; ++sub) {
         uint32_t pk[32];
         if (out32) {

@@ -71,6 +71,40 @@ BWG_HD void raster_tile(int t, int num_m_tiles, int num_n_tiles, int group_m, in
   *n_tile = r / rows;
 }
 
+// Wave-quantisation split.  With T output tiles on C persistent workers the
+// last wave holds only R = T mod C tiles.  When R <= C/2, each of those R
+// tiles is split along N into two halves (the MMA N drops from tile_n to
+// tile_n/2 in the instruction descriptor, the MegaMoE page's dynamic N), so
+// the last wave holds 2R half tiles and lasts about half a tile.  Returns the
+// number of split tiles (0: no split); the schedule then has T + R units.
+BWG_HD int tail_split_count(int T, int C) {
+  if (C <= 0 || T <= 0) return 0;
+  const int R = T % C;
+  return (R > 0 && 2 * R <= C) ? R : 0;
+}
+
+// Unit u of a schedule of T tiles whose last R tiles are split in two:
+// the tile index (in the tile order), the column offset inside the tile and
+// the unit's width in columns.
+BWG_HD void unit_tile(int u, int T, int R, int tile_n, int* tile, int* col_off, int* width) {
+  const int full = T - R;
+  if (u < full) {
+    *tile = u;
+    *col_off = 0;
+    *width = tile_n;
+  } else {
+    const int v = u - full;
+    *tile = full + v / 2;
+    *col_off = (v & 1) * (tile_n / 2);
+    *width = tile_n / 2;
+  }
+}
+
+// The instruction descriptor with its N field replaced (N a multiple of 16).
+BWG_HD uint32_t idesc_with_n(uint32_t idesc, uint32_t n) {
+  return (idesc & ~(0x3Fu << 17)) | ((n >> 3) << 17);
+}
+
 // Grouped (expert) schedule.  From the offsets of groups g0 .. g0+G-1 build
 //   prefix[g] = tiles of groups before g (prefix[G] = all tiles),
 //   lo[g], hi[g] = the group's row range, clamped into [0, M] and made

@@ -43,7 +43,7 @@ class PlanInfo(ctypes.Structure):
                 ("stages", ctypes.c_int), ("tiles", ctypes.c_int), ("k_blocks", ctypes.c_int),
                 ("coverage", ctypes.c_double), ("smem_input_per_cta", ctypes.c_int),
                 ("smem_total", ctypes.c_int), ("grid", ctypes.c_int), ("tx_bytes", ctypes.c_uint32),
-                ("idesc", ctypes.c_uint32)]
+                ("idesc", ctypes.c_uint32), ("units", ctypes.c_int)]
 
 
 def lib() -> ctypes.CDLL:
@@ -91,6 +91,10 @@ def lib() -> ctypes.CDLL:
             L.bwg_grouped_schedule.restype = i
             L.bwg_grouped_tile.argtypes = [i, i, ip, ip, ip, i, ip, ip, ip, ip]
             L.bwg_grouped_tile.restype = None
+            L.bwg_tail_split.argtypes = [i, i]
+            L.bwg_tail_split.restype = i
+            L.bwg_unit_tile.argtypes = [i, i, i, i, ip, ip, ip]
+            L.bwg_unit_tile.restype = None
             L.bwg_version.argtypes = []
             L.bwg_version.restype = ctypes.c_char_p
             _lib = L

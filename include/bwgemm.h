@@ -151,6 +151,8 @@ typedef struct {
   int grid;                /* CTAs launched for `sm_count` SMs */
   uint32_t tx_bytes;       /* bytes the stage barrier expects per k-block */
   uint32_t idesc;          /* instruction descriptor */
+  int units;               /* work units: tiles, plus one more for every last-wave tile
+                              split in two along N (see bwg_tail_split) */
 } bwg_plan_info;
 
 /*
@@ -191,6 +193,15 @@ int bwg_grouped_schedule(const int* offsets, int G, int M_total, int N, int tile
 /* Tile t of that schedule: group, first row, first column, row end. */
 void bwg_grouped_tile(int t, int G, const int* prefix, const int* lo, const int* hi, int tile_m,
                       int* g, int* m0, int* n0, int* row_end);
+
+/* Last-wave split of the persistent schedule: with T tiles on C workers,
+ * the number of tiles of the last, partly filled wave that are each split in
+ * two halves along N (0 when the remainder is more than half a wave). */
+int bwg_tail_split(int T, int C);
+
+/* Unit u of that schedule: tile index, column offset inside the tile and
+ * width in columns (tile_n, or tile_n/2 for the split tiles). */
+void bwg_unit_tile(int u, int T, int R, int tile_n, int* tile, int* col_off, int* width);
 
 /* Library version string. */
 const char* bwg_version(void);

@@ -187,3 +187,19 @@ def test_small_m_method_workload_full():
     D, _ = gpu_gemm(c.A, c.B, c.out_dtype)
     Dref, S = oracle.gemm(wl.bits(c.A), wl.bits(c.B))
     assert_within_bound(D, Dref, S, c.name)
+
+
+@pytest.mark.parametrize("kind", ["2cta", "1cta"])
+def test_last_wave_split_matches_unsplit(kind, monkeypatch):
+    """Half-width last-wave units (dynamic MMA N) give the same exact result
+    as whole tiles; 2304 tiles of 128 or 256 rows leave a remainder that is
+    split on both kernels."""
+    g = wl.generator(5300)
+    A = wl.randint_matrix(640, 512, -2, 2, g)
+    B = wl.randint_matrix(512, 2304, -2, 2, g)
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+    D1, _ = gpu_gemm(A, B, wl.OUT_FP32, kind)
+    assert np.array_equal(D1.double().numpy(), Dref)
+    monkeypatch.setenv("BWG_NO_TAIL_SPLIT", "1")
+    D2, _ = gpu_gemm(A, B, wl.OUT_FP32, kind)
+    assert np.array_equal(D2.double().numpy(), Dref)

@@ -207,3 +207,37 @@ def test_grouped_schedule_flags_bad_offsets(ops):
     assert _schedule(ops, [3, 10, 20], 256, 256)[0] == 0         # first != 0
     ok, prefix, lo, hi = _schedule(ops, [0, 10, 5, 20], 256, 256)
     assert all(l <= h for l, h in zip(lo, hi)) and lo[1] >= hi[0]  # clamped, disjoint
+
+
+@pytest.mark.parametrize("T,C", [(1024, 76), (256, 76), (1, 76), (76, 76), (77, 76), (114, 76),
+                                 (115, 76), (2048, 152), (5, 4), (40, 76)])
+def test_last_wave_split_covers_every_column_once(ops, T, C):
+    R = ops.lib().bwg_tail_split(T, C)
+    rem = T % C
+    assert R == (rem if 0 < rem and 2 * rem <= C else 0)
+    units = T + R
+    tile, off, width = (ctypes.c_int() for _ in range(3))
+    cover = {}
+    last_wave = (units - 1) // C
+    for u in range(units):
+        ops.lib().bwg_unit_tile(u, T, R, 256, ctypes.byref(tile), ctypes.byref(off), ctypes.byref(width))
+        assert width.value in (256, 128)
+        if width.value == 128:
+            assert u // C == last_wave  # split units all run in the last wave
+        for c in range(off.value, off.value + width.value, 64):
+            cover[(tile.value, c)] = cover.get((tile.value, c), 0) + 1
+    assert sorted(cover) == [(t, c) for t in range(T) for c in range(0, 256, 64)]
+    assert set(cover.values()) == {1}
+    # the split never lengthens the schedule and shortens it whenever it applies
+    waves_before = -(-T // C)
+    waves_after = ((T - R) // C + 0.5) if R else waves_before  # in whole-tile times
+    assert waves_after <= waves_before
+    if R:
+        assert waves_after == waves_before - 0.5
+
+
+def test_plan_reports_split_units(ops):
+    big = ops.plan(8192, 8192, 8192)
+    assert big.tiles == 1024 and big.units == 1024 + 1024 % 76
+    mid = ops.plan(4096, 4096, 4096)
+    assert mid.units == 256 + 256 % 76
