@@ -425,7 +425,7 @@ def run_ours(args, rank, world, local):
 
     variants = None
     if not args.no_variants:
-        variants = measure_variants(ops, wl, stream, dist_mod, peaks, min(args.steps, 100))
+        variants = measure_variants(ops, wl, stream, dist_mod, peaks, min(args.steps, 200))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -453,7 +453,9 @@ def run_ours(args, rank, world, local):
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
-        "launch_ms": {"mean": mean_launch, "median": statistics.median(per), "min": min(per), "max": max(per)},
+        "launch_ms": {"mean": mean_launch, "median": statistics.median(per), "min": min(per), "max": max(per),
+                      "first_tenth_mean": statistics.mean(per[:max(1, len(per) // 10)]),
+                      "last_tenth_mean": statistics.mean(per[-max(1, len(per) // 10):])},
         "variants": variants,
     }
     print(json.dumps(line), flush=True)
@@ -462,8 +464,8 @@ def run_ours(args, rank, world, local):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=3500)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

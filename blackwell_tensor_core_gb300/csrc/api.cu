@@ -85,7 +85,16 @@ std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
 int dense_stage_bytes(int cg) { return kRowsPerCta * kBK * 2 + (kTileN / cg) * kBK * 2; }
 
-int dense_smem(int cg, int stages) { return 1024 + stages * dense_stage_bytes(cg) + kEpiBytes + kBarrierArea; }
+int dense_smem(int cg, int stages, bool direct_store = false) {
+  return 1024 + stages * dense_stage_bytes(cg) + (direct_store ? 0 : kEpiBytes) + kBarrierArea;
+}
+
+// Epilogue choice: "tma" (staged boxes + TMA stores) or "direct" (rows stored
+// from registers, which frees the staging space for one more ring stage).
+bool direct_store_from_env() {
+  const char* v = std::getenv("BWG_EPILOGUE");
+  return v != nullptr && !std::strcmp(v, "direct");
+}
 
 int small_m_pad(int M) { return std::max(16, (M + 15) & ~15); }
 
@@ -98,6 +107,12 @@ int small_m_smem(int m_pad, int out_dtype, int stages) {
 }
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+int group_m_from_env() {
+  const char* v = std::getenv("BWG_GROUP_M");
+  const int g = v ? std::atoi(v) : 0;
+  return g > 0 ? g : kGroupM;
+}
 
 int no_tail_split_from_env() {
   const char* v = std::getenv("BWG_NO_TAIL_SPLIT");
@@ -144,18 +159,19 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     o->idesc = make_idesc_f16(fmt, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, m_pad);
   } else {
     const int cg = (kind == BWG_KERNEL_2CTA) ? 2 : 1;
+    const bool direct = direct_store_from_env();
     o->tile_m = kRowsPerCta * cg;
     o->tile_n = kTileN;
     o->mma_m = kRowsPerCta * cg;
     o->mma_n = kTileN;
-    const int fixed = dense_smem(cg, 0);
+    const int fixed = dense_smem(cg, 0, direct);
     int stages = std::min(8, (max_smem - fixed) / dense_stage_bytes(cg));
     if (force_stages > 0) stages = force_stages;
-    if (stages < 2 || dense_smem(cg, stages) > max_smem) return BWG_ERR_UNSUPPORTED;
+    if (stages < 2 || dense_smem(cg, stages, direct) > max_smem) return BWG_ERR_UNSUPPORTED;
     o->stages = stages;
     o->tiles = ceil_div(M, o->tile_m) * ceil_div(N, o->tile_n);
     o->smem_input_per_cta = stages * dense_stage_bytes(cg);
-    o->smem_total = dense_smem(cg, stages);
+    o->smem_total = dense_smem(cg, stages, direct);
     if (cg == 2)
       o->grid = 2 * std::min(o->tiles, max_clusters_2cta > 0 ? max_clusters_2cta : sm_count / 2);
     else
@@ -382,12 +398,13 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
   p.num_m_tiles = ceil_div(M, pl.tile_m);
   p.num_n_tiles = ceil_div(N, pl.tile_n);
   p.num_k_blocks = pl.k_blocks;
-  p.group_m = kGroupM;
+  p.group_m = group_m_from_env();
   p.stages = pl.stages;
   p.out_dtype = out_dtype;
   p.idesc = pl.idesc;
   p.tx_extra = g_tx_extra.load();
   p.no_tail_split = no_tail_split_from_env();
+  p.direct_store = direct_store_from_env() ? 1 : 0;
   if (pl.kernel == BWG_KERNEL_2CTA)
     return launch_status(launch_gemm_2cta(p, pl.grid, pl.smem_total, stream));
   return launch_status(launch_gemm_1cta(p, pl.grid, pl.smem_total, stream));

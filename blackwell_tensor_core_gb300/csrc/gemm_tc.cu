@@ -130,7 +130,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
   const uint32_t smem_a = base;
   const uint32_t smem_b = smem_a + S * kAStageBytes;
   const uint32_t smem_epi = smem_b + S * kBStageBytes;
-  const uint32_t smem_bar = smem_epi + kEpiBytes;
+  const uint32_t smem_bar = smem_epi + (p.direct_store ? 0u : static_cast<uint32_t>(kEpiBytes));
   auto full_bar = [&](int s) { return smem_bar + 8u * s; };
   auto empty_bar = [&](int s) { return smem_bar + 8u * (S + s); };
   auto acc_full_bar = [&](int a) { return smem_bar + 8u * (2 * S + a); };
@@ -329,7 +329,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         }
         const int col0 = tl.n0 + sub * sub_cols;
         if (col0 >= p.N) continue;
-        const bool whole_box = !GROUPED || (row_w + 32 <= tl.row_end);
+        const bool whole_box = !p.direct_store && (!GROUPED || (row_w + 32 <= tl.row_end));
         if (whole_box) {
           if (lane == 0) bulk_wait_group_read<1>();
           __syncwarp();
@@ -346,7 +346,8 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
           }
           buf ^= 1u;
         } else {
-          // Ragged end of a group: each thread stores its own row, if inside.
+          // Ragged end of a group, or the register-store epilogue: each
+          // thread stores its own row (64 or 32 columns), if inside.
           const int row = row_w + static_cast<int>(lane);
           if (row < tl.row_end) {
             const int elt = out32 ? 4 : 2;

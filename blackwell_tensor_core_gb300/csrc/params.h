@@ -48,6 +48,7 @@ struct GemmParams {
   uint32_t tx_extra;         // test hook: extra bytes expected per stage (0 normally)
   int G, g_begin, G_total;   // grouped only: groups in this launch, first group, all groups
   int no_tail_split;         // 1: never split last-wave tiles (tests and measurements)
+  int direct_store;          // 1: epilogue stores rows from registers (no staging, one more stage)
 };
 
 struct GroupedParams {
