@@ -56,6 +56,7 @@ struct DeviceState {
   int max_smem = 0;
   unsigned long long* err = nullptr;
   int clusters_2cta = 0;
+  int clusters_mc = 0;  // 4-CTA clusters (two pairs)
   int ctas_1cta = 0;
   int clusters_grouped = 0;
 };
@@ -121,7 +122,7 @@ int no_tail_split_from_env() {
 
 bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_count, int max_smem,
                       int force_kernel, int force_stages, int max_clusters_2cta, int max_ctas_1cta,
-                      bwg_plan_info* o) {
+                      int max_clusters_mc, bwg_plan_info* o) {
   std::memset(o, 0, sizeof(*o));
   if (M == 0 || N == 0) {
     o->kernel = BWG_KERNEL_NONE;
@@ -133,7 +134,8 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
   }
   int kind = force_kernel;
   if (kind == 0) kind = (M <= kSmallMMaxM) ? BWG_KERNEL_SMALL_M : BWG_KERNEL_2CTA;
-  if (kind != BWG_KERNEL_1CTA && kind != BWG_KERNEL_2CTA && kind != BWG_KERNEL_SMALL_M)
+  if (kind != BWG_KERNEL_1CTA && kind != BWG_KERNEL_2CTA && kind != BWG_KERNEL_SMALL_M &&
+      kind != BWG_KERNEL_2CTA_MC)
     return BWG_ERR_INVALID_ARG;
   if (kind == BWG_KERNEL_SMALL_M && M > kSmallMMaxM) return BWG_ERR_UNSUPPORTED;
   const uint32_t fmt = fp16_in ? kFmtF16 : kFmtBF16;
@@ -158,7 +160,8 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     o->tx_bytes = static_cast<uint32_t>(small_m_stage_bytes(m_pad));
     o->idesc = make_idesc_f16(fmt, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, m_pad);
   } else {
-    const int cg = (kind == BWG_KERNEL_2CTA) ? 2 : 1;
+    const int cg = (kind == BWG_KERNEL_1CTA) ? 1 : 2;
+    const int mc = (kind == BWG_KERNEL_2CTA_MC) ? 2 : 1;  // pairs per cluster
     const bool direct = direct_store_from_env();
     o->tile_m = kRowsPerCta * cg;
     o->tile_n = kTileN;
@@ -172,18 +175,26 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     o->tiles = ceil_div(M, o->tile_m) * ceil_div(N, o->tile_n);
     o->smem_input_per_cta = stages * dense_stage_bytes(cg);
     o->smem_total = dense_smem(cg, stages, direct);
-    if (cg == 2)
+    if (mc == 2) {
+      // schedule units are stacks of two pair tiles; 4-CTA clusters
+      const int units = ceil_div(ceil_div(M, o->tile_m), 2) * ceil_div(N, o->tile_n);
+      o->grid = 4 * std::min(units, max_clusters_mc > 0 ? max_clusters_mc : sm_count / 4);
+    } else if (cg == 2) {
       o->grid = 2 * std::min(o->tiles, max_clusters_2cta > 0 ? max_clusters_2cta : sm_count / 2);
-    else
+    } else {
       o->grid = std::min(o->tiles, max_ctas_1cta > 0 ? max_ctas_1cta : sm_count);
+    }
     o->tx_bytes = static_cast<uint32_t>(cg * dense_stage_bytes(cg));
     o->idesc = make_idesc_f16(fmt, /*a_mn_major=*/false, /*b_mn_major=*/true, o->mma_m, kTileN);
   }
   o->coverage = static_cast<double>(M) * N / (static_cast<double>(o->tiles) * o->tile_m * o->tile_n);
   o->units = o->tiles;
-  if (kind != BWG_KERNEL_SMALL_M && !no_tail_split_from_env()) {
-    const int workers = kind == BWG_KERNEL_2CTA ? o->grid / 2 : o->grid;
-    o->units = o->tiles + tail_split_count(o->tiles, workers);
+  if (kind != BWG_KERNEL_SMALL_M) {
+    const int per_unit = kind == BWG_KERNEL_2CTA_MC ? 2 : 1;
+    const int base_units = ceil_div(ceil_div(M, o->tile_m), per_unit) * ceil_div(N, o->tile_n);
+    const int workers = kind == BWG_KERNEL_2CTA ? o->grid / 2
+                        : kind == BWG_KERNEL_2CTA_MC ? o->grid / 4 : o->grid;
+    o->units = base_units + (no_tail_split_from_env() ? 0 : tail_split_count(base_units, workers));
   }
   return BWG_OK;
 }
@@ -262,9 +273,11 @@ bwg_status ensure_device(DeviceState** out) {
         st.init_status = BWG_ERR_CUDA;
       } else {
         st.clusters_2cta = max_active_clusters_gemm(2, false, dense_smem(2, 6));
+        st.clusters_mc = max_active_clusters_gemm(4, false, dense_smem(2, 6));
         st.clusters_grouped = max_active_clusters_gemm(2, true, dense_smem(2, 6));
         st.ctas_1cta = max_active_clusters_gemm(1, false, dense_smem(1, 4));
         if (st.clusters_2cta <= 0) st.clusters_2cta = st.sm_count / 2;
+        if (st.clusters_mc <= 0) st.clusters_mc = st.sm_count / 4;
         if (st.clusters_grouped <= 0) st.clusters_grouped = st.sm_count / 2;
         if (st.ctas_1cta <= 0) st.ctas_1cta = st.sm_count;
       }
@@ -316,6 +329,7 @@ int force_kernel_from_env() {
   if (v == nullptr) return 0;
   if (!std::strcmp(v, "1cta")) return BWG_KERNEL_1CTA;
   if (!std::strcmp(v, "2cta")) return BWG_KERNEL_2CTA;
+  if (!std::strcmp(v, "2cta_mc")) return BWG_KERNEL_2CTA_MC;
   if (!std::strcmp(v, "small_m")) return BWG_KERNEL_SMALL_M;
   return 0;
 }
@@ -346,7 +360,7 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
   if ((s = ensure_device(&st)) != BWG_OK) return s;
   bwg_plan_info pl;
   s = plan_dense(M, N, K, out_dtype, fp16_in, st->sm_count, st->max_smem, force_kernel_from_env(),
-                 force_stages_from_env(), st->clusters_2cta, st->ctas_1cta, &pl);
+                 force_stages_from_env(), st->clusters_2cta, st->ctas_1cta, st->clusters_mc, &pl);
   if (s != BWG_OK) return s;
   if (pl.kernel == BWG_KERNEL_ZERO)
     return launch_status(launch_zero_fill(D, M, N, ldd, out_elt(out_dtype), stream));
@@ -407,6 +421,8 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
   p.direct_store = direct_store_from_env() ? 1 : 0;
   if (pl.kernel == BWG_KERNEL_2CTA)
     return launch_status(launch_gemm_2cta(p, pl.grid, pl.smem_total, stream));
+  if (pl.kernel == BWG_KERNEL_2CTA_MC)
+    return launch_status(launch_gemm_2cta_mc(p, pl.grid, pl.smem_total, stream));
   return launch_status(launch_gemm_1cta(p, pl.grid, pl.smem_total, stream));
 }
 
@@ -567,7 +583,7 @@ bwg_status bwg_plan(int M, int N, int K, int out_dtype, int sm_count, int force_
   if (out_dtype != BWG_OUT_BF16 && out_dtype != BWG_OUT_FP32 && out_dtype != BWG_OUT_FP16)
     return BWG_ERR_INVALID_ARG;
   // 227 KiB of opt-in shared memory per block on sm_100-family parts.
-  return plan_dense(M, N, K, out_dtype, false, sm_count, 232448, force_kernel, force_stages, 0, 0,
+  return plan_dense(M, N, K, out_dtype, false, sm_count, 232448, force_kernel, force_stages, 0, 0, 0,
                     out);
 }
 

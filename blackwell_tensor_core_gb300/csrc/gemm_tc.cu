@@ -60,23 +60,29 @@ struct Tile {
   int g;
 };
 
-template <int CG, bool GROUPED>
+// MC pairs per cluster (1, or 2 when the pairs share B through TMA multicast):
+// a schedule unit is then a stack of MC tiles along M with the same columns,
+// and pair `pair` of the cluster takes tile row (unit row * MC + pair).
+template <int CG, int MC, bool GROUPED>
 struct Sched {
   static constexpr int kTileM = kRowsPerCta * CG;
   const GemmParams& p;
   const int* prefix;  // grouped tables in shared memory: prefix[G+1], lo[G], hi[G]
   const int* lo;
   const int* hi;
-  int tiles;          // whole tiles
-  int split;          // tiles of the last wave split in two along N
+  int pair;           // this CTA's pair inside the cluster
+  int rows_of_units;  // unit rows (tile rows / MC, rounded up)
+  int tiles;          // whole units
+  int split;          // units of the last wave split in two along N
 
   __device__ Sched(const GemmParams& p_, const int* prefix_, const int* lo_, const int* hi_,
-                   int workers)
-      : p(p_), prefix(prefix_), lo(lo_), hi(hi_) {
+                   int workers, int pair_)
+      : p(p_), prefix(prefix_), lo(lo_), hi(hi_), pair(pair_) {
+    rows_of_units = (p.num_m_tiles + MC - 1) / MC;
     if constexpr (GROUPED)
       tiles = prefix[p.G];
     else
-      tiles = p.num_m_tiles * p.num_n_tiles;
+      tiles = rows_of_units * p.num_n_tiles;
     split = p.no_tail_split ? 0 : tail_split_count(tiles, workers);
   }
 
@@ -90,8 +96,8 @@ struct Sched {
       grouped_tile(t, p.G, prefix, lo, hi, kTileM, kTileN, &tl.g, &tl.m0, &tl.n0, &tl.row_end);
     } else {
       int mt, nt;
-      raster_tile(t, p.num_m_tiles, p.num_n_tiles, p.group_m, &mt, &nt);
-      tl.m0 = mt * kTileM;
+      raster_tile(t, rows_of_units, p.num_n_tiles, (p.group_m + MC - 1) / MC, &mt, &nt);
+      tl.m0 = (mt * MC + pair) * kTileM;
       tl.n0 = nt * kTileN;
       tl.row_end = p.M;
       tl.g = 0;
@@ -116,13 +122,16 @@ __device__ __forceinline__ const CUtensorMap* b_map(const PT& P, int g) {
     return &P.map_b;
 }
 
-template <int CG, bool GROUPED, class PT>
+template <int CG, int MC, bool GROUPED, class PT>
 __device__ void gemm_body(const PT& P, const GemmParams& p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+  const uint32_t crank = (CG == 2) ? cluster_ctarank() : 0u;  // rank in the cluster
+  const uint32_t rank = crank & 1u;                             // rank in the CTA pair
+  const uint32_t pair = crank >> 1;                             // pair in the cluster (MC == 2)
+  const uint32_t leader = crank & ~1u;                          // the pair's MMA-issuing CTA
   const int S = p.stages;
   constexpr uint32_t kBCols = kTileN / CG;             // B columns a CTA loads for a whole tile
   constexpr uint32_t kBStageBytes = kBCols * kBK * 2;  // 32 KiB (1 CTA) or 16 KiB (pair)
@@ -142,7 +151,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), MC);  // one MMA commit per pair (multicast writes need both)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(acc_full_bar(a), 1);
@@ -159,7 +168,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
     if (threadIdx.x == 64) {
       const bool ok = grouped_tables(p.group_offsets, p.g_begin, p.G, p.G_total, p.M,
                                      p.num_n_tiles, kRowsPerCta * CG, t_prefix, t_lo, t_hi);
-      if (!ok && rank == 0) record_fault(p.err, kFaultBadOffsets, 0, 0, 0, 0);
+      if (!ok && crank == 0) record_fault(p.err, kFaultBadOffsets, 0, 0, 0, 0);
     }
   }
   if (warp == 0 && lane == 0) {
@@ -181,7 +190,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
 
   const int first = static_cast<int>((CG == 2) ? cluster_id_x() : blockIdx.x);
   const int stride = static_cast<int>((CG == 2) ? num_clusters_x() : gridDim.x);
-  const Sched<CG, GROUPED> sched(p, t_prefix, t_lo, t_hi, stride);
+  const Sched<CG, MC, GROUPED> sched(p, t_prefix, t_lo, t_hi, stride, static_cast<int>(pair));
   const int total = sched.total();
   bool aborted = false;
 
@@ -209,10 +218,19 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
           const int k0 = kb * kBK;
           if constexpr (CG == 2) {
             if (rank == 0) mbar_arrive_expect_tx(full_bar(s), stage_tx);
-            const uint32_t fb = mapa_shared(full_bar(s), 0);
+            const uint32_t fb = mapa_shared(full_bar(s), leader);
             tma_load_2d_pair(sa, &p.map_a, fb, k0, a_row);
-            for (uint32_t j = 0; j < b_chunks; ++j)
-              tma_load_2d_pair(sb + j * kBChunkBytes, mb, fb, b_col + 64 * j, k0);
+            if constexpr (MC == 1) {
+              for (uint32_t j = 0; j < b_chunks; ++j)
+                tma_load_2d_pair(sb + j * kBChunkBytes, mb, fb, b_col + 64 * j, k0);
+            } else {
+              // The pairs share B: box j of this CTA's columns is fetched once, by
+              // pair j, and multicast to the same-rank CTA of every pair; each
+              // destination's bytes complete on its own pair leader's barrier.
+              const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (rank + 2)));
+              for (uint32_t j = pair; j < b_chunks; j += MC)
+                tma_load_2d_pair_mc(sb + j * kBChunkBytes, mb, fb, b_col + 64 * j, k0, mask);
+            }
           } else {
             mbar_arrive_expect_tx(full_bar(s), stage_tx);
             tma_load_2d(sa, &p.map_a, full_bar(s), k0, a_row);
@@ -229,6 +247,11 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
     __syncwarp();
   } else if (warp == 1) {
     // ---- MMA issuer: one thread of CTA 0 drives the tensor cores -----------
+    // Commit masks: the stage-empty signal must reach every CTA whose shared
+    // memory the next loads of that stage write (all pairs when B is
+    // multicast); the accumulator-full signal only this pair.
+    const uint16_t empty_mask = static_cast<uint16_t>(MC == 2 ? 0xF : 0x3);
+    const uint16_t acc_mask = static_cast<uint16_t>(0x3u << (2 * pair));
     if (rank == 0 && lane == 0) {
       int s = 0;
       uint32_t ph = 0;
@@ -261,7 +284,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
                         (kb | kk) != 0 ? 1u : 0u);
           }
           if constexpr (CG == 2)
-            mma_commit_pair_mc(empty_bar(s), 0x3);
+            mma_commit_pair_mc(empty_bar(s), empty_mask);
           else
             mma_commit_1cta(empty_bar(s));
           if (++s == S) {
@@ -271,7 +294,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         }
         if (aborted) break;
         if constexpr (CG == 2)
-          mma_commit_pair_mc(acc_full_bar(acc), 0x3);
+          mma_commit_pair_mc(acc_full_bar(acc), acc_mask);
         else
           mma_commit_1cta(acc_full_bar(acc));
         if (++acc == 2) {
@@ -285,7 +308,8 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
     // ---- epilogue: TMEM -> registers -> convert -> swizzled SMEM -> TMA -----
     const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may read
     const uint32_t ebuf = smem_epi + (warp - 2u) * 2u * kEpiBufBytes;
-    const uint32_t acc_empty_leader0 = (CG == 2) ? mapa_shared(acc_empty_bar(0), 0) : acc_empty_bar(0);
+    const uint32_t acc_empty_leader0 =
+        (CG == 2) ? mapa_shared(acc_empty_bar(0), leader) : acc_empty_bar(0);
     const bool out32 = p.out_dtype == kOutF32;
     const bool outbf = p.out_dtype == kOutBF16;
     int acc = 0;
@@ -400,14 +424,14 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
   }
 }
 
-template <int CG>
+template <int CG, int MC>
 __global__ void __launch_bounds__(kThreads, 1) gemm_dense_kernel(const __grid_constant__ GemmParams p) {
-  gemm_body<CG, false>(p, p);
+  gemm_body<CG, MC, false>(p, p);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_grouped_kernel(const __grid_constant__ GroupedParams p) {
-  gemm_body<2, true>(p, p.base);
+  gemm_body<2, 1, true>(p, p.base);
 }
 
 template <class K, class P>
@@ -430,11 +454,15 @@ cudaError_t launch_cluster(K kernel, const P& p, int cg, int grid, size_t smem, 
 }  // namespace
 
 cudaError_t launch_gemm_1cta(const GemmParams& p, int grid, size_t smem, cudaStream_t s) {
-  return launch_cluster(gemm_dense_kernel<1>, p, 1, grid, smem, s);
+  return launch_cluster(gemm_dense_kernel<1, 1>, p, 1, grid, smem, s);
 }
 
 cudaError_t launch_gemm_2cta(const GemmParams& p, int grid, size_t smem, cudaStream_t s) {
-  return launch_cluster(gemm_dense_kernel<2>, p, 2, grid, smem, s);
+  return launch_cluster(gemm_dense_kernel<2, 1>, p, 2, grid, smem, s);
+}
+
+cudaError_t launch_gemm_2cta_mc(const GemmParams& p, int grid, size_t smem, cudaStream_t s) {
+  return launch_cluster(gemm_dense_kernel<2, 2>, p, 4, grid, smem, s);
 }
 
 cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, cudaStream_t s) {
@@ -461,16 +489,18 @@ static int occupancy_clusters(const void* fn, int cg, size_t smem) {
   return n;
 }
 
-int max_active_clusters_gemm(int cg, bool grouped, size_t smem) {
+int max_active_clusters_gemm(int cluster, bool grouped, size_t smem) {
   const void* fn = grouped ? reinterpret_cast<const void*>(gemm_grouped_kernel)
-                           : (cg == 2 ? reinterpret_cast<const void*>(gemm_dense_kernel<2>)
-                                      : reinterpret_cast<const void*>(gemm_dense_kernel<1>));
-  return occupancy_clusters(fn, cg, smem);
+                   : cluster == 4 ? reinterpret_cast<const void*>(gemm_dense_kernel<2, 2>)
+                   : cluster == 2 ? reinterpret_cast<const void*>(gemm_dense_kernel<2, 1>)
+                                  : reinterpret_cast<const void*>(gemm_dense_kernel<1, 1>);
+  return occupancy_clusters(fn, cluster, smem);
 }
 
 cudaError_t set_gemm_attributes(size_t smem) {
-  const void* fns[3] = {reinterpret_cast<const void*>(gemm_dense_kernel<1>),
-                        reinterpret_cast<const void*>(gemm_dense_kernel<2>),
+  const void* fns[4] = {reinterpret_cast<const void*>(gemm_dense_kernel<1, 1>),
+                        reinterpret_cast<const void*>(gemm_dense_kernel<2, 1>),
+                        reinterpret_cast<const void*>(gemm_dense_kernel<2, 2>),
                         reinterpret_cast<const void*>(gemm_grouped_kernel)};
   for (const void* fn : fns) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -71,12 +71,13 @@ struct SmallMParams {
 // Host launchers (one per kernel instantiation).  They only enqueue.
 cudaError_t launch_gemm_1cta(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_gemm_2cta(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_gemm_2cta_mc(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_small_m(const SmallMParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_zero_fill(void* d, int rows, int cols, int ld, int elt_bytes, cudaStream_t s);
 
 // Occupancy helpers: co-resident clusters (or CTAs) for a given launch shape.
-int max_active_clusters_gemm(int cg, bool grouped, size_t smem);
+int max_active_clusters_gemm(int cluster, bool grouped, size_t smem);
 int max_active_ctas_small_m(size_t smem);
 
 }  // namespace bwg

@@ -157,6 +157,18 @@ BWG_DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar
       : "memory");
 }
 
+// Pair form with cluster multicast: the box lands at offset `dst` in every
+// CTA of `cta_mask`, and each destination's bytes complete on the barrier at
+// offset `bar` in that destination's pair-leader CTA (`bar` addresses a leader).
+BWG_DEV void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                                 int32_t c1, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
+      : "memory");
+}
+
 // 2-D tiled store from this CTA's shared memory (bulk-group completion).
 BWG_DEV void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1) {
   asm volatile(

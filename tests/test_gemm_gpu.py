@@ -24,7 +24,7 @@ def _built():
 
 # ---------------------------------------------------------------- exact ----
 
-@pytest.mark.parametrize("kind", ["2cta", "1cta"])
+@pytest.mark.parametrize("kind", ["2cta", "1cta", "2cta_mc"])
 def test_tile_case_exact(kind):
     """256x256x512 integers in {-2..2}, FP32 out: every partial sum is an
     integer below 2^24, so the result is exact in any summation order."""
@@ -34,7 +34,7 @@ def test_tile_case_exact(kind):
     assert np.array_equal(D.double().numpy(), Dref)
 
 
-@pytest.mark.parametrize("kind", ["2cta", "1cta"])
+@pytest.mark.parametrize("kind", ["2cta", "1cta", "2cta_mc"])
 @pytest.mark.parametrize("out", [wl.OUT_BF16, wl.OUT_FP16])
 def test_integer_inputs_rounded_output_exact(kind, out):
     g = wl.generator(2001)
@@ -63,7 +63,7 @@ SHAPES = [(520, 600, 456), (300, 264, 72), (129, 8, 8), (256, 256, 64), (1000, 1
           (257, 520, 40), (768, 1024, 2048)]
 
 
-@pytest.mark.parametrize("kind", ["2cta", "1cta"])
+@pytest.mark.parametrize("kind", ["2cta", "1cta", "2cta_mc"])
 @pytest.mark.parametrize("shape", SHAPES)
 def test_random_shapes_within_bound(kind, shape):
     M, N, K = shape
@@ -89,7 +89,7 @@ def test_small_m_within_bound(shape, out):
     assert_within_bound(D, Dref, S, "small_m %s out=%d" % (shape, out))
 
 
-@pytest.mark.parametrize("kind", ["2cta", "1cta", None])
+@pytest.mark.parametrize("kind", ["2cta", "1cta", "2cta_mc", None])
 def test_fp16_inputs(kind):
     M = 72 if kind is None else 400
     g = wl.generator(5000)
@@ -101,7 +101,7 @@ def test_fp16_inputs(kind):
         assert_within_bound(D, Dref, S, "fp16 in %s out=%d" % (kind, out))
 
 
-@pytest.mark.parametrize("kind", ["2cta", "1cta", None])
+@pytest.mark.parametrize("kind", ["2cta", "1cta", "2cta_mc", None])
 def test_leading_dimensions_and_untouched_padding(kind):
     M = 90 if kind is None else 300
     N, K = 200, 136
@@ -189,7 +189,7 @@ def test_small_m_method_workload_full():
     assert_within_bound(D, Dref, S, c.name)
 
 
-@pytest.mark.parametrize("kind", ["2cta", "1cta"])
+@pytest.mark.parametrize("kind", ["2cta", "1cta", "2cta_mc"])
 def test_last_wave_split_matches_unsplit(kind, monkeypatch):
     """Half-width last-wave units (dynamic MMA N) give the same exact result
     as whole tiles; 2304 tiles of 128 or 256 rows leave a remainder that is
@@ -205,7 +205,7 @@ def test_last_wave_split_matches_unsplit(kind, monkeypatch):
     assert np.array_equal(D2.double().numpy(), Dref)
 
 
-@pytest.mark.parametrize("kind", ["2cta", "1cta"])
+@pytest.mark.parametrize("kind", ["2cta", "1cta", "2cta_mc"])
 @pytest.mark.parametrize("out", [wl.OUT_FP32, wl.OUT_BF16])
 def test_register_store_epilogue(kind, out, monkeypatch):
     """The epilogue that stores rows straight from registers (seven-stage
@@ -221,3 +221,14 @@ def test_register_store_epilogue(kind, out, monkeypatch):
     else:
         assert_bits_equal(D, oracle.round_to(Dref, "bf16"), "direct bf16")
     assert torch.all(full[:, 600:] == 9.0)
+
+
+def test_multicast_kernel_at_8192_sampled():
+    """The two-pair multicast kernel on the 8192^3 workload (odd and even
+    unit rows, last-wave split) on sampled outputs and seam rows."""
+    c = wl.large_case()
+    D, _ = gpu_gemm(c.A, c.B, c.out_dtype, "2cta_mc")
+    _check_sampled(c.A, c.B, D, 8000, 14, c.name + " multicast")
+    for r in (255, 256, 511, 512):
+        Dref, S = oracle.gemm(wl.bits(c.A[r:r + 1]), wl.bits(c.B))
+        assert_within_bound(D[r:r + 1], Dref, S, "row %d" % r)
