@@ -82,6 +82,68 @@ struct MapKeyHash {
 };
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
+// Stream-K workspace of the small-M kernel, one per (device, stream): FP32
+// partial accumulators and per-tile arrival counters.  Counters are zeroed
+// when the buffer is made and every call leaves them at zero again.  A
+// workspace is reused only by calls on its own stream, so calls on one stream
+// are ordered; calls on different streams use different workspaces.
+struct Workspace {
+  float* ws = nullptr;
+  int* counters = nullptr;
+  size_t ws_bytes = 0;
+  int n_counters = 0;
+};
+std::unordered_map<unsigned long long, Workspace> g_workspaces;
+
+bwg_status get_workspace(cudaStream_t stream, size_t ws_bytes, int n_counters, Workspace* out) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const unsigned long long key =
+      (static_cast<unsigned long long>(dev) << 56) ^ reinterpret_cast<uintptr_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  Workspace& w = g_workspaces[key];
+  if (w.ws_bytes < ws_bytes || w.n_counters < n_counters) {
+    // grow to cover both the old and the new request, so that alternating
+    // shapes settle on one buffer instead of reallocating every call
+    const size_t wb = std::max(ws_bytes, w.ws_bytes);
+    const int nc = std::max(n_counters, w.n_counters);
+    if (w.ws != nullptr || w.counters != nullptr) {
+      // the old buffers may still be in use by work queued on this stream
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return BWG_ERR_CUDA;
+      cudaFree(w.ws);
+      cudaFree(w.counters);
+      w = Workspace();
+    }
+    if (cudaMalloc(&w.ws, wb) != cudaSuccess ||
+        cudaMalloc(&w.counters, static_cast<size_t>(nc) * sizeof(int)) != cudaSuccess ||
+        cudaMemsetAsync(w.counters, 0, static_cast<size_t>(nc) * sizeof(int), stream) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(w.ws);
+      cudaFree(w.counters);
+      w = Workspace();
+      return BWG_ERR_CUDA;
+    }
+    w.ws_bytes = wb;
+    w.n_counters = nc;
+  }
+  *out = w;
+  return BWG_OK;
+}
+
+// Most CTAs that share one tile under the stream-K split.
+int streamk_max_sharers(int tiles, int kb, int grid) {
+  const long long W = static_cast<long long>(tiles) * kb;
+  int most = 1;
+  for (int t = 0; t < tiles; ++t) {
+    int first = 0, count = 1;
+    streamk_tile_workers(t, kb, W, grid, &first, &count);
+    most = std::max(most, count);
+  }
+  return most;
+}
+
+
+
 // ------------------------------------------------------------ planning -----
 
 int dense_stage_bytes(int cg) { return kRowsPerCta * kBK * 2 + (kTileN / cg) * kBK * 2; }
@@ -153,10 +215,26 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     if (force_stages > 0) stages = force_stages;
     if (stages < 2 || small_m_smem(m_pad, out_dtype, stages) > max_smem) return BWG_ERR_UNSUPPORTED;
     o->stages = stages;
-    o->tiles = ceil_div(N, 128);
     o->smem_input_per_cta = stages * small_m_stage_bytes(m_pad);
     o->smem_total = small_m_smem(m_pad, out_dtype, stages);
-    o->grid = std::min(o->tiles, sm_count);
+    // 128 columns per tile by default: narrower strides start B's boxes off a
+    // 128-byte boundary, which measured slower than leaving SMs idle.
+    int tn = 128;
+    if (const char* v = std::getenv("BWG_SMALL_M_TILE_N")) {
+      const int f = std::atoi(v);
+      if (f >= 16 && f <= 128 && f % 16 == 0) tn = f;
+    }
+    o->tile_n = tn;
+    o->tiles = ceil_div(N, tn);
+    const long long iters = static_cast<long long>(o->tiles) * o->k_blocks;
+    // Stream-K pays when whole tiles would need a partly filled second wave,
+    // or fill at most half the SMs; in between, whole tiles walking K in step
+    // measured faster.
+    int streamk = (o->tiles % sm_count != 0 && (o->tiles > sm_count || 2 * o->tiles <= sm_count) &&
+                   iters >= sm_count) ? 1 : 0;
+    if (const char* v = std::getenv("BWG_STREAMK")) streamk = (v[0] == '1' && iters >= sm_count) ? 1 : 0;
+    o->streamk = streamk;
+    o->grid = streamk ? sm_count : std::min(o->tiles, sm_count);
     o->tx_bytes = static_cast<uint32_t>(small_m_stage_bytes(m_pad));
     o->idesc = make_idesc_f16(fmt, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, m_pad);
   } else {
@@ -375,9 +453,14 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
         !get_map(&p.map_at, A, in_t, K, M, static_cast<uint64_t>(lda) * 2, kBK, m_pad,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !get_map(&p.map_d, D, out_map_dtype(out_dtype), N, M, static_cast<uint64_t>(ldd) * oe, 64,
-                 m_pad, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !get_map(&p.map_d, D, out_map_dtype(out_dtype), N, M, static_cast<uint64_t>(ldd) * oe,
+                 std::min(64, pl.tile_n), m_pad, CU_TENSOR_MAP_SWIZZLE_NONE))
       return BWG_ERR_CUDA;
+    if (pl.tile_n > 64 &&
+        !get_map(&p.map_d2, D, out_map_dtype(out_dtype), N, M, static_cast<uint64_t>(ldd) * oe,
+                 pl.tile_n - 64, m_pad, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return BWG_ERR_CUDA;
+    p.tile_n = pl.tile_n;
     p.err = st->err;
     p.timeout_ns = g_timeout_ns.load();
     p.M = M;
@@ -390,6 +473,15 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
     p.out_dtype = out_dtype;
     p.idesc = pl.idesc;
     p.tx_extra = g_tx_extra.load();
+    p.streamk = pl.streamk;
+    if (pl.streamk) {
+      p.ws_slots = streamk_max_sharers(pl.tiles, pl.k_blocks, pl.grid);
+      Workspace w;
+      const size_t ws_bytes = static_cast<size_t>(pl.tiles) * p.ws_slots * m_pad * 128 * sizeof(float);
+      if ((s = get_workspace(stream, ws_bytes, pl.tiles, &w)) != BWG_OK) return s;
+      p.ws = w.ws;
+      p.ws_counters = w.counters;
+    }
     return launch_status(launch_small_m(p, pl.grid, pl.smem_total, stream));
   }
   GemmParams p;
@@ -623,6 +715,12 @@ int bwg_tail_split(int T, int C) { return tail_split_count(T, C); }
 
 void bwg_unit_tile(int u, int T, int R, int tile_n, int* tile, int* col_off, int* width) {
   unit_tile(u, T, R, tile_n, tile, col_off, width);
+}
+
+long long bwg_streamk_begin(int i, long long W, int C) { return streamk_begin(i, W, C); }
+
+void bwg_streamk_tile_workers(int t, int kb, long long W, int C, int* first, int* count) {
+  streamk_tile_workers(t, kb, W, C, first, count);
 }
 
 const char* bwg_version(void) { return "bwgemm 0.1 (sm_103a)"; }

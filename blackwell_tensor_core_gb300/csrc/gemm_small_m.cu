@@ -14,13 +14,26 @@
 // box of m_pad rows x 64 K.  The accumulator has TMEM lane = output column and
 // TMEM column = row of D, so each epilogue thread owns one output column and
 // writes it down the rows of a [m_pad x 64] staging tile, which a TMA store
-// then writes to D (rows >= M are clipped by the tensor bounds).  This avoids
-// the in-TMEM transpose the page describes: no transpose is needed when the
-// staging tile is written column-wise.
+// then writes to D (rows >= M are clipped by the tensor bounds).  No transpose
+// step is needed when the staging tile is written column-wise.
 //
-// Work split: one 128-column tile per CTA step, persistent over tiles, a ring
-// of `stages` k-blocks, two accumulator slots.  The path is HBM-bound (B is
-// read once, A is re-read from L2 by every CTA).
+// Work split.  The path is bound by HBM (B is read once).  Two ways keep all
+// SMs streaming:
+//  - a narrower tile stride: a tile stores tile_n <= 128 output columns (the
+//    MMA and the loads still span 128, the extra columns come from L2 since
+//    the neighbouring tile reads them at the same time), so N/tile_n tiles
+//    fill the SMs while every CTA walks K in step with the others and the
+//    CTAs together read whole rows of B from DRAM;
+//  - stream-K, when there are more tiles than SMs or far fewer: the
+//    (tile, k-block) iterations are shared out evenly over all CTAs; a CTA
+//    works through one or more "segments" (a tile and a range of its
+//    k-blocks).  A segment that covers a whole tile is stored directly.
+// The CTAs sharing a tile each write their FP32 partial accumulator to a
+// workspace slot (slot = CTA index - first CTA of the tile), then increment
+// the tile's counter; the CTA that brings the counter to the number of
+// sharers sums the slots in slot order (deterministic), stores D and resets
+// the counter.  No CTA ever waits for another.  With stream-K off, segments
+// are whole tiles taken persistently (tile = CTA index + i * grid).
 #include "layout.h"
 #include "params.h"
 #include "ptx.cuh"
@@ -40,6 +53,44 @@ __device__ __forceinline__ void record_fault_small(unsigned long long* err, uint
                                   ((stage & 0xFFu) << 8) | (phase & 0xFFu);
   atomicCAS(err, 0ull, code);
 }
+
+// The segments of this CTA, in order.
+struct Segments {
+  const SmallMParams& p;
+  long long W;        // all iterations (stream-K)
+  long long lo, hi;   // this CTA's iterations (stream-K)
+
+  __device__ explicit Segments(const SmallMParams& p_) : p(p_) {
+    W = static_cast<long long>(p.num_tiles) * p.num_k_blocks;
+    lo = streamk_begin(blockIdx.x, W, gridDim.x);
+    hi = streamk_begin(blockIdx.x + 1, W, gridDim.x);
+  }
+
+  // Segment i: false when there is none.
+  __device__ bool get(int i, int* t, int* kb0, int* kb1) const {
+    if (!p.streamk) {
+      const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+      if (tile >= p.num_tiles) return false;
+      *t = tile;
+      *kb0 = 0;
+      *kb1 = p.num_k_blocks;
+      return true;
+    }
+    long long pos = lo;
+    for (int j = 0; j < i && pos < hi; ++j) {
+      const long long tile = pos / p.num_k_blocks;
+      const long long end = (tile + 1) * p.num_k_blocks;
+      pos = end < hi ? end : hi;
+    }
+    if (pos >= hi) return false;
+    const long long tile = pos / p.num_k_blocks;
+    const long long end = (tile + 1) * p.num_k_blocks < hi ? (tile + 1) * p.num_k_blocks : hi;
+    *t = static_cast<int>(tile);
+    *kb0 = static_cast<int>(pos - tile * p.num_k_blocks);
+    *kb1 = static_cast<int>(end - tile * p.num_k_blocks);
+    return true;
+  }
+};
 
 __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_constant__ SmallMParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -61,6 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
   auto acc_full_bar = [&](int a) { return smem_bar + 8u * (2 * S + a); };
   auto acc_empty_bar = [&](int a) { return smem_bar + 8u * (2 * S + 2 + a); };
   const uint32_t tmem_slot = smem_bar + 8u * (2 * S + 4);
+  const uint32_t last_flag = tmem_slot + 4u;  // "this CTA finishes the tile" broadcast
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -77,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
     prefetch_tensormap(&p.map_bt);
     prefetch_tensormap(&p.map_at);
     prefetch_tensormap(&p.map_d);
+    if (p.tile_n > 64) prefetch_tensormap(&p.map_d2);
   }
   if (warp == 1) {
     tmem_alloc<1>(tmem_slot, kTmemCols);
@@ -86,6 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = ld_shared_u32(tmem_slot);
+  const Segments segs(p);
   bool aborted = false;
 
   if (warp == 0) {
@@ -93,9 +147,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
       int s = 0;
       uint32_t ph = 0;
       const uint32_t tx = stage_bytes + p.tx_extra;
-      for (int t = blockIdx.x; t < p.num_tiles && !aborted; t += gridDim.x) {
-        const int n0 = t * 128;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+      int t, kb0, kb1;
+      for (int i = 0; !aborted && segs.get(i, &t, &kb0, &kb1); ++i) {
+        const int n0 = t * p.tile_n;
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, p.timeout_ns)) {
             record_fault_small(p.err, 0, 1, s, ph ^ 1u);
             aborted = true;
@@ -121,7 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
       uint32_t ph = 0;
       int acc = 0;
       uint32_t acc_ph = 0;
-      for (int t = blockIdx.x; t < p.num_tiles && !aborted; t += gridDim.x) {
+      int t, kb0, kb1;
+      for (int i = 0; !aborted && segs.get(i, &t, &kb0, &kb1); ++i) {
         if (!mbar_wait(acc_empty_bar(acc), acc_ph ^ 1u, p.timeout_ns)) {
           record_fault_small(p.err, 1, 3, acc, acc_ph ^ 1u);
           aborted = true;
@@ -129,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * 256u;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(full_bar(s), ph, p.timeout_ns)) {
             record_fault_small(p.err, 1, 0, s, ph);
             aborted = true;
@@ -144,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
 #pragma unroll
           for (uint32_t kk = 0; kk < kBK / 16; ++kk)
             mma_f16<1>(d_tmem, a_desc + ((kk * 2048u) >> 4), b_desc + ((kk * 32u) >> 4), p.idesc,
-                       (kb | kk) != 0 ? 1u : 0u);
+                       (kb > kb0 || kk > 0) ? 1u : 0u);
           mma_commit_1cta(empty_bar(s));
           if (++s == S) {
             s = 0;
@@ -164,15 +220,46 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
     // Epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = output columns.
     const uint32_t q = warp & 3u;
     const uint32_t ch = q * 32u + lane;              // column within the 128-wide tile
-    const uint32_t half = ch >> 6;                   // which 64-column staging tile
+    const uint32_t half = ch >> 6;                   // which staging tile: columns 0-63, 64-127
     const uint32_t col_in_half = ch & 63u;
+    const bool stores = static_cast<int>(ch) < p.tile_n;  // column is part of this tile's output
+    const uint32_t pitch = half == 0 ? static_cast<uint32_t>(min(64, p.tile_n))
+                                     : static_cast<uint32_t>(max(p.tile_n - 64, 1));
     const bool out32 = p.out_dtype == kOutF32;
     const bool outbf = p.out_dtype == kOutBF16;
     const bool store_thread = threadIdx.x == 64;     // first epilogue thread issues TMA stores
+    const size_t slot_floats = static_cast<size_t>(p.m_pad) * 128u;
     int acc = 0;
     uint32_t acc_ph = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      const int n0 = t * 128;
+    int t, kb0, kb1;
+
+    // One value of D (row r, this thread's column) into the staging tile.
+    // Staging half h is a dense [m_pad][pitch_h] tile, pitch_0 = min(64, tile_n),
+    // pitch_1 = tile_n - 64: exactly the box of the TMA store that writes it.
+    auto stage_value = [&](int r, float x) {
+      if (!stores) return;
+      const uint32_t tile = smem_d + half * half_bytes;
+      if (out32) {
+        st_shared_u32(tile + (static_cast<uint32_t>(r) * pitch + col_in_half) * 4u, __float_as_uint(x));
+      } else {
+        const uint32_t h = outbf ? pack_bf16x2(x, 0.f) : pack_f16x2(x, 0.f);
+        st_shared_u16(tile + (static_cast<uint32_t>(r) * pitch + col_in_half) * 2u,
+                      static_cast<uint16_t>(h & 0xFFFFu));
+      }
+    };
+    auto store_staged = [&](int n0) {
+      fence_proxy_async_shared();
+      named_bar_sync(1, 128);
+      if (store_thread) {
+        tma_store_2d(&p.map_d, smem_d, n0, 0);
+        if (p.tile_n > 64 && n0 + 64 < p.N) tma_store_2d(&p.map_d2, smem_d + half_bytes, n0 + 64, 0);
+        bulk_commit_group();
+      }
+    };
+
+    for (int i = 0; segs.get(i, &t, &kb0, &kb1); ++i) {
+      const int n0 = t * p.tile_n;
+      const bool whole = (kb0 == 0 && kb1 == p.num_k_blocks);
       const bool seen = mbar_wait(acc_full_bar(acc), acc_ph, p.timeout_ns);
       // The four epilogue warps share the staging tile: they go on only if all
       // 128 threads saw the accumulator complete.
@@ -182,10 +269,16 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
         break;
       }
       tc_fence_after();
-      // The previous tile's TMA store must have finished reading the staging tile.
+      // The previous TMA store must have finished reading the staging tile.
       if (store_thread) bulk_wait_group_read<0>();
       named_bar_sync(1, 128);
       const uint32_t t_acc = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc) * 256u;
+      int first = 0, sharers = 1;
+      float* slot = nullptr;
+      if (!whole) {
+        streamk_tile_workers(t, p.num_k_blocks, segs.W, gridDim.x, &first, &sharers);
+        slot = p.ws + (static_cast<size_t>(t) * p.ws_slots + (blockIdx.x - first)) * slot_floats;
+      }
       for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(t_acc + c0, v);
@@ -196,30 +289,56 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
           if (lane == 0) mbar_arrive_local(acc_empty_bar(acc));
         }
         const int rows = min(32, p.M - c0);
-        const uint32_t tile = smem_d + half * half_bytes;
-        if (out32) {
+        if (whole) {
 #pragma unroll
           for (int r = 0; r < 32; ++r)
-            if (r < rows)
-              st_shared_u32(tile + (static_cast<uint32_t>(c0 + r) * 64u + col_in_half) * 4u, v[r]);
+            if (r < rows) stage_value(c0 + r, __uint_as_float(v[r]));
         } else {
+          // partial accumulator -> workspace slot, [row][128 columns] FP32
 #pragma unroll
-          for (int r = 0; r < 32; ++r) {
-            if (r < rows) {
-              const float x = __uint_as_float(v[r]);
-              const uint32_t h = outbf ? pack_bf16x2(x, 0.f) : pack_f16x2(x, 0.f);
-              st_shared_u16(tile + (static_cast<uint32_t>(c0 + r) * 64u + col_in_half) * 2u,
-                            static_cast<uint16_t>(h & 0xFFFFu));
-            }
-          }
+          for (int r = 0; r < 32; ++r)
+            if (r < rows) slot[static_cast<size_t>(c0 + r) * 128u + ch] = __uint_as_float(v[r]);
         }
       }
-      fence_proxy_async_shared();
-      named_bar_sync(1, 128);
-      if (store_thread) {
-        tma_store_2d(&p.map_d, smem_d, n0, 0);
-        if (n0 + 64 < p.N) tma_store_2d(&p.map_d, smem_d + half_bytes, n0 + 64, 0);
-        bulk_commit_group();
+      if (whole) {
+        store_staged(n0);
+      } else {
+        // Publish the partial, count it; the last sharer sums all slots.
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (store_thread) {
+          const int old = atomicAdd(p.ws_counters + t, 1);
+          const uint32_t is_last = (old == sharers - 1) ? 1u : 0u;
+          if (is_last) p.ws_counters[t] = 0;  // every sharer has arrived: ready for the next call
+          __threadfence();
+          st_shared_u32(last_flag, is_last);
+        }
+        named_bar_sync(1, 128);
+        if (ld_shared_u32(last_flag) != 0u) {
+          // Sum the slots in slot order, 32 rows at a time: per slot the 32
+          // loads of a thread are independent (and coalesced across the
+          // warp), so they are all in flight together.
+          const float* tile_slots = p.ws + static_cast<size_t>(t) * p.ws_slots * slot_floats;
+          for (int c0 = 0; c0 < p.M; c0 += 32) {
+            const int rows = min(32, p.M - c0);
+            float sum[32];
+#pragma unroll
+            for (int r = 0; r < 32; ++r) sum[r] = 0.f;
+            for (int sl = 0; sl < sharers; ++sl) {
+              const float* src = tile_slots + static_cast<size_t>(sl) * slot_floats +
+                                 static_cast<size_t>(c0) * 128u + ch;
+              float v[32];
+#pragma unroll
+              for (int r = 0; r < 32; ++r) v[r] = (r < rows) ? __ldcg(src + r * 128) : 0.f;
+#pragma unroll
+              for (int r = 0; r < 32; ++r) sum[r] += v[r];
+            }
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+              if (r < rows) stage_value(c0 + r, sum[r]);
+          }
+          store_staged(n0);
+        }
       }
       if (++acc == 2) {
         acc = 0;

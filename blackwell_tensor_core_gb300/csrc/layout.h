@@ -105,6 +105,31 @@ BWG_HD uint32_t idesc_with_n(uint32_t idesc, uint32_t n) {
   return (idesc & ~(0x3Fu << 17)) | ((n >> 3) << 17);
 }
 
+// Stream-K split: W = tiles * kb k-block iterations of a tile list shared out
+// evenly over C workers; worker i owns iterations [begin(i), begin(i+1)).  A
+// tile whose iterations fall to several workers is finished by the last of
+// them to arrive, which sums the partial accumulators in worker order.
+BWG_HD long long streamk_begin(int i, long long W, int C) {
+  return (W * static_cast<long long>(i)) / C;
+}
+
+// The worker whose range holds iteration p (0 <= p < W).
+BWG_HD int streamk_owner(long long p, long long W, int C) {
+  int i = static_cast<int>((p * C) / W);
+  if (i >= C) i = C - 1;
+  while (i > 0 && streamk_begin(i, W, C) > p) --i;
+  while (i + 1 < C && streamk_begin(i + 1, W, C) <= p) ++i;
+  return i;
+}
+
+// Workers sharing tile t (kb iterations per tile): the first one and how many.
+BWG_HD void streamk_tile_workers(int t, int kb, long long W, int C, int* first, int* count) {
+  const int a = streamk_owner(static_cast<long long>(t) * kb, W, C);
+  const int b = streamk_owner(static_cast<long long>(t + 1) * kb - 1, W, C);
+  *first = a;
+  *count = b - a + 1;
+}
+
 // Grouped (expert) schedule.  From the offsets of groups g0 .. g0+G-1 build
 //   prefix[g] = tiles of groups before g (prefix[G] = all tiles),
 //   lo[g], hi[g] = the group's row range, clamped into [0, M] and made

@@ -59,13 +59,19 @@ struct GroupedParams {
 struct SmallMParams {
   CUtensorMap map_bt;  // B [K, N] viewed as the MMA's MN-major A: box {64 (N), 64 (K)}
   CUtensorMap map_at;  // A [M, K] as the MMA's K-major B: box {64 (K), m_pad (rows)}
-  CUtensorMap map_d;   // D [M, N], box {64 (N), m_pad (rows)}, no swizzle
+  CUtensorMap map_d;   // D [M, N], box {min(64, tile_n) (N), m_pad (rows)}, no swizzle
+  CUtensorMap map_d2;  // D [M, N], box {tile_n - 64 (N), m_pad}, when tile_n > 64
   unsigned long long* err;
   unsigned long long timeout_ns;
   int M, N, K, m_pad;
+  int tile_n;          // output columns per tile (<= 128; the MMA always spans 128)
   int num_tiles, num_k_blocks, stages, out_dtype;
   uint32_t idesc;
   uint32_t tx_extra;
+  int streamk;       // 1: (tile, k-block) iterations shared evenly over the grid
+  int ws_slots;      // partial-accumulator slots per tile (most CTAs sharing a tile)
+  float* ws;         // stream-K partials: [num_tiles][ws_slots][m_pad][128] FP32
+  int* ws_counters;  // stream-K arrival counters, one per tile, zero between calls
 };
 
 // Host launchers (one per kernel instantiation).  They only enqueue.

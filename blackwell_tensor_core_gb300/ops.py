@@ -43,7 +43,7 @@ class PlanInfo(ctypes.Structure):
                 ("stages", ctypes.c_int), ("tiles", ctypes.c_int), ("k_blocks", ctypes.c_int),
                 ("coverage", ctypes.c_double), ("smem_input_per_cta", ctypes.c_int),
                 ("smem_total", ctypes.c_int), ("grid", ctypes.c_int), ("tx_bytes", ctypes.c_uint32),
-                ("idesc", ctypes.c_uint32), ("units", ctypes.c_int)]
+                ("idesc", ctypes.c_uint32), ("units", ctypes.c_int), ("streamk", ctypes.c_int)]
 
 
 def lib() -> ctypes.CDLL:
@@ -95,6 +95,10 @@ def lib() -> ctypes.CDLL:
             L.bwg_tail_split.restype = i
             L.bwg_unit_tile.argtypes = [i, i, i, i, ip, ip, ip]
             L.bwg_unit_tile.restype = None
+            L.bwg_streamk_begin.argtypes = [i, ctypes.c_longlong, i]
+            L.bwg_streamk_begin.restype = ctypes.c_longlong
+            L.bwg_streamk_tile_workers.argtypes = [i, i, ctypes.c_longlong, i, ip, ip]
+            L.bwg_streamk_tile_workers.restype = None
             L.bwg_version.argtypes = []
             L.bwg_version.restype = ctypes.c_char_p
             _lib = L

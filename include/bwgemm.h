@@ -55,6 +55,9 @@ typedef enum { BWG_OUT_BF16 = 0, BWG_OUT_FP32 = 1, BWG_OUT_FP16 = 2 } bwg_out_dt
  *   lda >= K, ldb >= N, ldd >= N.  M, N or K == 0: M or N == 0 is a no-op;
  *   K == 0 writes D = 0.  Sizes above 2^31-1 elements per dimension are not
  *   supported.  Returns BWG_OK once the work is enqueued.
+ *   The small-M kernel may share a tile's k-blocks among several CTAs; it then
+ *   uses a device workspace that the library allocates (cudaMalloc) on the
+ *   first such call on a stream and keeps for later calls on that stream.
  */
 bwg_status gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K, int lda, int ldb,
                      int ldd, int out_dtype, void* stream);
@@ -141,7 +144,8 @@ typedef enum {
 
 typedef struct {
   int kernel;              /* bwg_kernel_kind */
-  int tile_m, tile_n, tile_k;
+  int tile_m, tile_n, tile_k; /* SMALL_M: tile_m = padded rows, tile_n = output columns per
+                                 tile (<= 128; the MMA spans 128) */
   int mma_m, mma_n;        /* shape of one tcgen05.mma (mma_n = padded M for SMALL_M) */
   int stages;              /* SMEM ring depth */
   int tiles;               /* output tiles */
@@ -154,6 +158,8 @@ typedef struct {
   uint32_t idesc;          /* instruction descriptor */
   int units;               /* work units: tiles, plus one more for every last-wave tile
                               split in two along N (see bwg_tail_split) */
+  int streamk;             /* SMALL_M: 1 if (tile, k-block) iterations are shared evenly
+                              over all CTAs (partial tiles summed through a workspace) */
 } bwg_plan_info;
 
 /*
@@ -203,6 +209,12 @@ int bwg_tail_split(int T, int C);
 /* Unit u of that schedule: tile index, column offset inside the tile and
  * width in columns (tile_n, or tile_n/2 for the split tiles). */
 void bwg_unit_tile(int u, int T, int R, int tile_n, int* tile, int* col_off, int* width);
+
+/* Stream-K schedule of the small-M kernel (host copy, for tests): with
+ * `tiles` tiles of `kb` k-blocks on C CTAs, the first iteration CTA i owns,
+ * and for tile t the first CTA sharing it and how many CTAs share it. */
+long long bwg_streamk_begin(int i, long long W, int C);
+void bwg_streamk_tile_workers(int t, int kb, long long W, int C, int* first, int* count);
 
 /* Library version string. */
 const char* bwg_version(void);

@@ -232,3 +232,71 @@ def test_multicast_kernel_at_8192_sampled():
     for r in (255, 256, 511, 512):
         Dref, S = oracle.gemm(wl.bits(c.A[r:r + 1]), wl.bits(c.B))
         assert_within_bound(D[r:r + 1], Dref, S, "row %d" % r)
+
+
+# --------------------------------------------------- small-M stream-K ------
+
+@pytest.mark.parametrize("shape", [(72, 1000, 4096), (16, 128, 8192), (128, 4104, 640), (72, 16384, 512)])
+def test_small_m_streamk_exact_and_repeatable(shape, monkeypatch):
+    """Stream-K shares each tile's k-blocks among several CTAs (up to ~20
+    here); with integer inputs every partial sum is exact, so the result must
+    equal the oracle bit for bit, on every repeat (the per-tile counters reset
+    themselves) and with stream-K switched off."""
+    M, N, K = shape
+    g = wl.generator(5500 + M + N)
+    A = wl.randint_matrix(M, K, -1, 1, g)
+    B = wl.randint_matrix(K, N, -1, 1, g)
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+    for _ in range(3):
+        D, _ = gpu_gemm(A, B, wl.OUT_FP32, None)
+        assert np.array_equal(D.double().numpy(), Dref)
+    monkeypatch.setenv("BWG_STREAMK", "0")
+    D, _ = gpu_gemm(A, B, wl.OUT_FP32, None)
+    assert np.array_equal(D.double().numpy(), Dref)
+    monkeypatch.setenv("BWG_STREAMK", "1")
+    D, _ = gpu_gemm(A, B, wl.OUT_FP32, None)
+    assert np.array_equal(D.double().numpy(), Dref)
+
+
+def test_small_m_streamk_bf16_bound_and_growing_workspace(monkeypatch):
+    monkeypatch.setenv("BWG_STREAMK", "1")
+    for (M, N, K) in [(40, 256, 10240), (72, 6000, 2048), (100, 12000, 3000)]:
+        g = wl.generator(5600 + N)
+        A = wl.normal_matrix(M, K, 1.0, g)
+        B = wl.normal_matrix(K, N, 1.0, g)
+        Dref, S = oracle.gemm(wl.bits(A), wl.bits(B))
+        D, _ = gpu_gemm(A, B, wl.OUT_BF16, None)
+        assert_within_bound(D, Dref, S, "streamk %s" % ((M, N, K),))
+
+
+def test_small_m_streamk_on_a_side_stream():
+    from blackwell_tensor_core_gb300 import ops
+    g = wl.generator(5700)
+    A = wl.randint_matrix(72, 2048, -2, 2, g)
+    B = wl.randint_matrix(2048, 3000, -2, 2, g)
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+    s = torch.cuda.Stream()
+    Ad, Bd = A.cuda(), B.cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        D = ops.gemm(Ad, Bd, out_dtype=torch.float32, stream=s)
+    s.synchronize()
+    assert np.array_equal(D.cpu().double().numpy(), Dref)
+
+
+@pytest.mark.parametrize("tile_n", [64, 80, 112, 128])
+@pytest.mark.parametrize("out", [wl.OUT_BF16, wl.OUT_FP32])
+def test_small_m_tile_stride(tile_n, out, monkeypatch):
+    """Tiles that store fewer columns than the 128 the MMA spans: every
+    column written exactly once, ragged last tile clipped, padding untouched."""
+    monkeypatch.setenv("BWG_SMALL_M_TILE_N", str(tile_n))
+    g = wl.generator(5800 + tile_n)
+    A = wl.randint_matrix(72, 640, -2, 2, g)
+    B = wl.randint_matrix(640, 1000, -2, 2, g)
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+    D, full = gpu_gemm(A, B, out, None, ldd=1016, sentinel=5.0)
+    if out == wl.OUT_FP32:
+        assert np.array_equal(D.double().numpy(), Dref)
+    else:
+        assert_bits_equal(D, oracle.round_to(Dref, "bf16"), "tile_n %d" % tile_n)
+    assert torch.all(full[:, 1000:] == 5.0)

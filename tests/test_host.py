@@ -104,7 +104,11 @@ def test_planner_choices(ops):
     assert big.kernel == ops.KERNEL_2CTA and big.stages == 6 and big.tiles == 1024
     assert big.grid == 152 and big.smem_total <= 232448
     small = ops.plan(72, 16384, 7168)
-    assert small.kernel == ops.KERNEL_SMALL_M and small.mma_n == 80 and small.tiles == 128
+    assert small.kernel == ops.KERNEL_SMALL_M and small.mma_n == 80
+    # whole 128-column tiles walking K in step; stream-K for few or too many tiles
+    assert small.tile_n == 128 and small.tiles == 128 and small.streamk == 0 and small.grid == 128
+    assert ops.plan(72, 8192, 7168).streamk == 1 and ops.plan(72, 24576, 7168).streamk == 1
+    assert ops.plan(72, 19456, 7168).streamk == 0
     assert small.smem_total <= 232448 and small.stages >= 4
     for tokens, n in _golden()["n_compute"]:
         assert ops.plan(int(tokens), 4096, 4096).mma_n == n
@@ -241,3 +245,20 @@ def test_plan_reports_split_units(ops):
     assert big.tiles == 1024 and big.units == 1024 + 1024 % 76
     mid = ops.plan(4096, 4096, 4096)
     assert mid.units == 256 + 256 % 76
+
+
+@pytest.mark.parametrize("tiles,kb,C", [(128, 112, 152), (128, 112, 128), (3, 1, 152), (1, 200, 152),
+                                        (10, 7, 4), (300, 16, 152), (128, 2, 152)])
+def test_streamk_ranges_cover_each_tile_iteration_once(ops, tiles, kb, C):
+    L = ops.lib()
+    W = tiles * kb
+    begins = [L.bwg_streamk_begin(i, W, C) for i in range(C + 1)]
+    assert begins[0] == 0 and begins[-1] == W
+    assert all(b <= c for b, c in zip(begins, begins[1:]))
+    sizes = [c - b for b, c in zip(begins, begins[1:])]
+    assert max(sizes) - min(sizes) <= 1  # even shares
+    first, count = ctypes.c_int(), ctypes.c_int()
+    for t in range(tiles):
+        L.bwg_streamk_tile_workers(t, kb, W, C, ctypes.byref(first), ctypes.byref(count))
+        owners = sorted({i for i in range(C) for p in range(begins[i], begins[i + 1]) if t * kb <= p < (t + 1) * kb})
+        assert owners == list(range(first.value, first.value + count.value))
