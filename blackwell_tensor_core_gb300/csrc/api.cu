@@ -586,6 +586,123 @@ bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
   return BWG_OK;
 }
 
+// ------------------------------------------- no-allocation small-M path -----
+//
+// Some callers cannot let a library call cudaMalloc: code that runs while a
+// stream is being captured into a CUDA graph (allocation calls are not
+// allowed there), processes that hand all device memory to their own pool
+// allocator, and real-time loops that must not block on the allocator.  For
+// them gemm_bf16_small_m_noalloc runs the stream-K small-M kernel with its
+// partial sums and tile counters in the fixed device array below instead of
+// the per-stream workspace that gemm_bf16 allocates.
+//
+// The array is a plain global of the library: every GPU that loads the
+// library holds these 32 MiB until the process exits, all calls on a device
+// share them, and each call leaves its partial sums behind.  Calls whose GPU
+// work overlaps (different streams, no ordering between them) race on it.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // whole array
+constexpr size_t kNoAllocCounterBytes = size_t(64) << 10;   // tile counters: up to 16384 tiles
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the array for the current device.  The name
+// g_noalloc_scratch in host code is only a handle for the runtime, so the
+// address is looked up once per device (with that device current) and kept.
+bwg_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return launch_status(cudaErrorUnknown);
+  if (dev < 0 || dev >= kMaxDevices) return BWG_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return BWG_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return BWG_OK;
+}
+
+// Tensor map without the descriptor cache (inserting into the cache would
+// allocate host memory).
+bool encode_map_direct(CUtensorMap* m, const void* ptr, CUtensorMapDataType dtype, uint64_t inner,
+                       uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                       CUtensorMapSwizzle swizzle) {
+  cuuint64_t gdim[2] = {inner, outer};
+  cuuint64_t gstride[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estride[2] = {1, 1};
+  return g_encode(m, dtype, 2, const_cast<void*>(ptr), gdim, gstride, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bwg_status run_small_m_noalloc(const void* A, const void* B, void* D, int M, int N, int K, int lda,
+                               int ldb, int ldd, int out_dtype, cudaStream_t stream) {
+  bwg_status s = check_args(A, B, D, M, N, K, lda, ldb, ldd, out_dtype);
+  if (s != BWG_OK) return s;
+  if (M == 0 || N == 0) return BWG_OK;
+  if (M > kSmallMMaxM) return BWG_ERR_UNSUPPORTED;
+  DeviceState* st = nullptr;
+  if ((s = ensure_device(&st)) != BWG_OK) return s;
+  if (K == 0) return launch_status(launch_zero_fill(D, M, N, ldd, out_elt(out_dtype), stream));
+  bwg_plan_info pl;
+  s = plan_dense(M, N, K, out_dtype, false, st->sm_count, st->max_smem, BWG_KERNEL_SMALL_M, 0,
+                 st->clusters_2cta, st->ctas_1cta, st->clusters_mc, &pl);
+  if (s != BWG_OK) return s;
+  // Always the stream-K form: every CTA gets at least one k-block.
+  const long long iters = static_cast<long long>(pl.tiles) * pl.k_blocks;
+  const int grid = static_cast<int>(std::min<long long>(st->sm_count, iters));
+  const int m_pad = pl.mma_n;
+  const int slots = streamk_max_sharers(pl.tiles, pl.k_blocks, grid);
+  const size_t counter_bytes = static_cast<size_t>(pl.tiles) * sizeof(int);
+  const size_t partial_bytes = static_cast<size_t>(pl.tiles) * slots * m_pad * 128 * sizeof(float);
+  if (counter_bytes > kNoAllocCounterBytes ||
+      partial_bytes > kNoAllocScratchBytes - kNoAllocCounterBytes)
+    return BWG_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  if ((s = noalloc_scratch(&scratch)) != BWG_OK) return s;
+  // The counters must start at zero; a call cut short by the watchdog could
+  // have left some behind, so clear the ones this call uses.
+  if (cudaMemsetAsync(scratch, 0, counter_bytes, stream) != cudaSuccess)
+    return launch_status(cudaErrorUnknown);
+  const CUtensorMapDataType in_t = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int oe = out_elt(out_dtype);
+  SmallMParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!encode_map_direct(&p.map_bt, B, in_t, N, K, static_cast<uint64_t>(ldb) * 2, 64, kBK,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_map_direct(&p.map_at, A, in_t, K, M, static_cast<uint64_t>(lda) * 2, kBK, m_pad,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_map_direct(&p.map_d, D, out_map_dtype(out_dtype), N, M,
+                         static_cast<uint64_t>(ldd) * oe, 64, m_pad, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_map_direct(&p.map_d2, D, out_map_dtype(out_dtype), N, M,
+                         static_cast<uint64_t>(ldd) * oe, 64, m_pad, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return BWG_ERR_CUDA;
+  p.err = st->err;
+  p.timeout_ns = g_timeout_ns.load();
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.m_pad = m_pad;
+  p.tile_n = 128;
+  p.num_tiles = pl.tiles;
+  p.num_k_blocks = pl.k_blocks;
+  p.stages = pl.stages;
+  p.out_dtype = out_dtype;
+  p.idesc = pl.idesc;
+  p.tx_extra = g_tx_extra.load();
+  p.streamk = 1;
+  p.ws_slots = slots;
+  p.ws_counters = static_cast<int*>(scratch);
+  p.ws = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + kNoAllocCounterBytes);
+  return launch_status(launch_small_m(p, grid, pl.smem_total, stream));
+}
+
 }  // namespace
 
 // ================================================================ C ABI ====
@@ -616,6 +733,12 @@ bwg_status grouped_gemm_fp16(const void* A, const void* const* B, void* D, const
                      static_cast<cudaStream_t>(stream));
 }
 
+bwg_status gemm_bf16_small_m_noalloc(const void* A, const void* B, void* D, int M, int N, int K,
+                                     int lda, int ldb, int ldd, int out_dtype, void* stream) {
+  return run_small_m_noalloc(A, B, D, M, N, K, lda, ldb, ldd, out_dtype,
+                             static_cast<cudaStream_t>(stream));
+}
+
 bwg_status gemm_bf16_host(const void* A_host, const void* B_host, void* D_host, int M, int N, int K,
                           int out_dtype, void* dA, void* dB, void* dD, void* stream) {
   if (M < 0 || N < 0 || K < 0) return BWG_ERR_INVALID_ARG;
@@ -642,6 +765,8 @@ const char* bwg_status_string(int status) {
     case BWG_ERR_UNSUPPORTED: return "unsupported device or size";
     case BWG_ERR_CUDA: return "CUDA runtime or driver error";
     case BWG_ERR_TIMEOUT: return "kernel barrier wait timed out";
+    case BWG_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than the fixed 32 MiB no-allocation buffer holds";
     default: return "unknown status";
   }
 }

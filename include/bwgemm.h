@@ -41,7 +41,8 @@ typedef enum {
   BWG_ERR_ALIGNMENT = 2,   /* pointer or leading dimension breaks the 16-byte rule */
   BWG_ERR_UNSUPPORTED = 3, /* device is not sm_103 / sm_100 family, or size beyond limits */
   BWG_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
-  BWG_ERR_TIMEOUT = 5      /* a kernel gave up waiting on a barrier (device error word) */
+  BWG_ERR_TIMEOUT = 5,     /* a kernel gave up waiting on a barrier (device error word) */
+  BWG_ERR_SCRATCH_LIMIT = 6 /* gemm_bf16_small_m_noalloc: problem too large for its fixed buffer */
 } bwg_status;
 
 typedef enum { BWG_OUT_BF16 = 0, BWG_OUT_FP32 = 1, BWG_OUT_FP16 = 2 } bwg_out_dtype;
@@ -88,6 +89,33 @@ bwg_status grouped_gemm_bf16(const void* A, const void* const* B, void* D, const
 /* Same as grouped_gemm_bf16 with FP16 inputs and FP16 output. */
 bwg_status grouped_gemm_fp16(const void* A, const void* const* B, void* D, const int* group_offsets,
                              int G, int M_total, int N, int K, void* stream);
+
+/*
+ * No-allocation form of gemm_bf16 for small M (M <= 128).  The pages have no
+ * counterpart: it exists for callers that cannot let the library call
+ * cudaMalloc -- code running while a stream is captured into a CUDA graph
+ * (allocation is not allowed there), programs that give all device memory to
+ * their own pool allocator, and latency-critical loops that must not wait on
+ * the allocator.  It computes what gemm_bf16 computes (same arguments and
+ * rules) with the stream-K small-M kernel, keeping that kernel's partial sums
+ * and per-tile counters in one fixed 32 MiB device array inside the library
+ * instead of an allocated workspace:
+ *   - the array exists on every GPU that loads the library, until exit;
+ *   - the first call on a device looks up the array's device address (a
+ *     runtime symbol lookup); make that first call before any stream capture;
+ *   - every call shares the array and leaves its contents behind; each call
+ *     clears the tile counters it needs (cudaMemsetAsync on `stream`), so
+ *     calls on one stream are safe, but calls whose GPU work overlaps (other
+ *     streams without ordering) race on the array;
+ *   - problems whose partial sums do not fit return BWG_ERR_SCRATCH_LIMIT:
+ *     with rows = M rounded up to 16, tiles = ceil(N/128) and S SMs, they
+ *     need tiles * sharers * rows * 128 * 4 bytes (at most 32 MiB - 64 KiB),
+ *     where sharers <= ceil(S / tiles) + 1 (3 when N = 16384 on 152 SMs),
+ *     and at most 16384 tiles; M > 128 returns BWG_ERR_UNSUPPORTED.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+bwg_status gemm_bf16_small_m_noalloc(const void* A, const void* B, void* D, int M, int N, int K,
+                                     int lda, int ldb, int ldd, int out_dtype, void* stream);
 
 /*
  * End-to-end convenience form of gemm_bf16 for host-resident data: copies
