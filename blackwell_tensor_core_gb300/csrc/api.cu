@@ -576,6 +576,14 @@ bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
     p.g_begin = g0;
     p.G_total = G;
     p.no_tail_split = no_tail_split_from_env();
+    p.idesc_swap = make_idesc_f16(fp16 ? kFmtF16 : kFmtBF16, true, false, 2 * kRowsPerCta, 16);
+    {
+      // Off by default: a swapped tile still loads whole A and B boxes, and
+      // tiles here are bound by how fast shared memory fills, so it measured
+      // no faster than the padded tile.  BWG_GROUPED_SWAP=1 turns it on.
+      const char* v = std::getenv("BWG_GROUPED_SWAP");
+      p.swap_ends = (v != nullptr && v[0] == '1') ? 1 : 0;
+    }
     // Upper bound on tiles: every group adds at most one partial row tile.
     const long long max_tiles =
         (static_cast<long long>(ceil_div(M_total, 2 * kRowsPerCta)) + gn) * p.num_n_tiles;
@@ -846,6 +854,10 @@ long long bwg_streamk_begin(int i, long long W, int C) { return streamk_begin(i,
 
 void bwg_streamk_tile_workers(int t, int kb, long long W, int C, int* first, int* count) {
   streamk_tile_workers(t, kb, W, C, first, count);
+}
+
+int bwg_grouped_swap_rows(int m0, int row_end, int tile_m) {
+  return grouped_swap_rows(m0, row_end, tile_m);
 }
 
 const char* bwg_version(void) { return "bwgemm 0.1 (sm_103a)"; }

@@ -55,9 +55,10 @@ __device__ __forceinline__ void record_fault(unsigned long long* err, unsigned l
 struct Tile {
   int m0;
   int n0;
-  int width;
+  int width;      // columns of the unit; 0 = nothing to do (second half of a swapped tile)
   int row_end;
   int g;
+  int swap_rows;  // > 0: rows m0 .. m0+swap_rows-1 computed with swapped operands
 };
 
 // MC pairs per cluster (1, or 2 when the pairs share B through TMA multicast):
@@ -92,8 +93,17 @@ struct Sched {
     Tile tl;
     int t, col_off;
     unit_tile(u, tiles, split, kTileN, &t, &col_off, &tl.width);
+    tl.swap_rows = 0;
     if constexpr (GROUPED) {
       grouped_tile(t, p.G, prefix, lo, hi, kTileM, kTileN, &tl.g, &tl.m0, &tl.n0, &tl.row_end);
+      if constexpr (CG == 2) {
+        if (p.swap_ends) tl.swap_rows = grouped_swap_rows(tl.m0, tl.row_end, kTileM);
+        // A swapped tile spans all 256 columns in one unit (its MMA M is the
+        // column count): if the last-wave split halved it, the first half
+        // does the whole tile and the second half nothing.
+        if (tl.swap_rows > 0 && tl.width != kTileN) tl.width = (col_off == 0) ? kTileN : 0;
+        if (tl.swap_rows > 0) col_off = 0;
+      }
     } else {
       int mt, nt;
       raster_tile(t, rows_of_units, p.num_n_tiles, (p.group_m + MC - 1) / MC, &mt, &nt);
@@ -201,10 +211,17 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
       uint32_t ph = 0;
       for (int t = first; t < total && !aborted; t += stride) {
         const Tile tl = sched.at(t);
+        if (tl.width == 0) continue;
         const uint32_t b_cols = static_cast<uint32_t>(tl.width) / CG;  // this CTA's B columns
         const uint32_t b_chunks = b_cols / 64;
+        // Swapped tile: A's rows are the MMA's N, split between the pair; each
+        // CTA loads only its half of the rounded-up rows, in 8-row boxes.
+        // (the whole 128-row box is loaded: fewer, larger requests measured
+        // faster than fetching only the rows used)
+        const uint32_t half_rows = static_cast<uint32_t>(((tl.swap_rows + 15) & ~15) / 2);
         const uint32_t stage_tx = CG * (kAStageBytes + b_cols * kBK * 2) + p.tx_extra;
-        const int a_row = tl.m0 + static_cast<int>(rank) * kRowsPerCta;
+        const int a_row = tl.swap_rows > 0 ? tl.m0 + static_cast<int>(rank * half_rows)
+                                           : tl.m0 + static_cast<int>(rank) * kRowsPerCta;
         const int b_col = tl.n0 + static_cast<int>(rank * b_cols);
         const CUtensorMap* mb = b_map<CG, GROUPED>(P, tl.g);
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
@@ -258,6 +275,8 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
       int acc = 0;
       uint32_t acc_ph = 0;
       for (int t = first; t < total && !aborted; t += stride) {
+        const Tile tl = sched.at(t);
+        if (tl.width == 0) continue;
         if (!mbar_wait(acc_empty_bar(acc), acc_ph ^ 1u, p.timeout_ns)) {
           record_fault(p.err, kFaultTimeout, kRoleMma, kBarAccEmpty, acc, acc_ph ^ 1u);
           aborted = true;
@@ -265,7 +284,12 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * kTileN;
-        const uint32_t idesc = idesc_with_n(p.idesc, static_cast<uint32_t>(sched.at(t).width));
+        const bool swapped = tl.swap_rows > 0;
+        // Swapped: MMA A = the B boxes (MN-major, 256 columns as M), MMA B =
+        // the A rows (K-major, N = rows rounded up to 16).
+        const uint32_t idesc =
+            swapped ? idesc_with_n(p.idesc_swap, static_cast<uint32_t>((tl.swap_rows + 15) & ~15))
+                    : idesc_with_n(p.idesc, static_cast<uint32_t>(tl.width));
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait(full_bar(s), ph, p.timeout_ns)) {
             record_fault(p.err, kFaultTimeout, kRoleMma, kBarFull, s, ph);
@@ -280,8 +304,9 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
           for (uint32_t kk = 0; kk < kBK / 16; ++kk) {
             // K-major A: the next 16 K values are 32 bytes further along each
             // 128-byte row.  MN-major B: they are 16 rows (2048 bytes) further.
-            mma_f16<CG>(d_tmem, a_desc + ((kk * 32u) >> 4), b_desc + ((kk * 2048u) >> 4), idesc,
-                        (kb | kk) != 0 ? 1u : 0u);
+            const uint64_t ad = a_desc + ((kk * 32u) >> 4);
+            const uint64_t bd = b_desc + ((kk * 2048u) >> 4);
+            mma_f16<CG>(d_tmem, swapped ? bd : ad, swapped ? ad : bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           if constexpr (CG == 2)
             mma_commit_pair_mc(empty_bar(s), empty_mask);
@@ -317,6 +342,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
     uint32_t buf = 0;
     for (int t = first; t < total; t += stride) {
       const Tile tl = sched.at(t);
+      if (tl.width == 0) continue;
       if (!warp_wait(acc_full_bar(acc), acc_ph, p.timeout_ns)) {
         if (lane == 0) record_fault(p.err, kFaultTimeout, kRoleEpilogue, kBarAccFull, acc, acc_ph);
         aborted = true;
@@ -325,6 +351,44 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
       tc_fence_after();
       const int row_w = tl.m0 + static_cast<int>(rank * kRowsPerCta + q * 32u);
       const uint32_t t_acc = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc) * kTileN;
+      if (GROUPED && tl.swap_rows > 0) {
+        // Swapped tile: TMEM lane = output column, TMEM column = row.  Each
+        // thread writes its column down the tile's valid rows; the 32 lanes
+        // of a warp write 32 adjacent columns of one row at a time.
+        const int col = tl.n0 + static_cast<int>(rank * kRowsPerCta + q * 32u + lane);
+        const int npad = (tl.swap_rows + 15) & ~15;
+        const int elt = out32 ? 4 : 2;
+        for (int c0 = 0; c0 < npad; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_acc + c0, v);
+          tmem_wait_ld();
+          if (c0 + 32 >= npad) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
+          }
+          if (col < p.N) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (c0 + j < tl.swap_rows) {
+                uint8_t* dst = static_cast<uint8_t*>(p.d_ptr) +
+                               (static_cast<size_t>(tl.m0 + c0 + j) * p.ldd + col) * elt;
+                const float x = __uint_as_float(v[j]);
+                if (out32)
+                  *reinterpret_cast<uint32_t*>(dst) = v[j];
+                else
+                  *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(
+                      (outbf ? pack_bf16x2(x, 0.f) : pack_f16x2(x, 0.f)) & 0xFFFFu);
+              }
+            }
+          }
+        }
+        if (++acc == 2) {
+          acc = 0;
+          acc_ph ^= 1u;
+        }
+        continue;
+      }
       const int sub_cols = out32 ? 32 : 64;
       const int nsub = tl.width / sub_cols;
       for (int sub = 0; sub < nsub; ++sub) {

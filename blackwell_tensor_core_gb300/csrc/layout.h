@@ -175,4 +175,15 @@ BWG_HD void grouped_tile(int t, int G, const int* prefix, const int* lo, const i
   *row_end = hi[g];
 }
 
+// Rows of a grouped tile at or below which it is computed with swapped
+// operands ("MegaMoE …" section 04: the short token side goes on the MMA's N,
+// rounded up to 16), instead of a 256-row tile that is mostly padding.
+constexpr int kSwapMaxRows = 128;
+
+// Valid rows of a grouped tile if it is computed swapped, else 0.
+BWG_HD int grouped_swap_rows(int m0, int row_end, int tile_m) {
+  const int rows = row_end - m0 < tile_m ? row_end - m0 : tile_m;
+  return rows <= kSwapMaxRows ? rows : 0;
+}
+
 }  // namespace bwg

@@ -49,6 +49,8 @@ struct GemmParams {
   int G, g_begin, G_total;   // grouped only: groups in this launch, first group, all groups
   int no_tail_split;         // 1: never split last-wave tiles (tests and measurements)
   int direct_store;          // 1: epilogue stores rows from registers (no staging, one more stage)
+  int swap_ends;             // grouped: 1 = compute group ends of <= 128 rows with swapped operands
+  uint32_t idesc_swap;       // grouped: descriptor of the swapped MMA (A MN-major, B K-major)
 };
 
 struct GroupedParams {

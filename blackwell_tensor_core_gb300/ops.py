@@ -99,6 +99,8 @@ def lib() -> ctypes.CDLL:
             L.bwg_streamk_begin.restype = ctypes.c_longlong
             L.bwg_streamk_tile_workers.argtypes = [i, i, ctypes.c_longlong, i, ip, ip]
             L.bwg_streamk_tile_workers.restype = None
+            L.bwg_grouped_swap_rows.argtypes = [i, i, i]
+            L.bwg_grouped_swap_rows.restype = i
             L.bwg_version.argtypes = []
             L.bwg_version.restype = ctypes.c_char_p
             _lib = L

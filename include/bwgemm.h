@@ -244,6 +244,11 @@ void bwg_unit_tile(int u, int T, int R, int tile_n, int* tile, int* col_off, int
 long long bwg_streamk_begin(int i, long long W, int C);
 void bwg_streamk_tile_workers(int t, int kb, long long W, int C, int* first, int* count);
 
+/* Valid rows of a grouped tile starting at row m0 of a group ending at
+ * row_end if the grouped kernel computes it with swapped operands (rows up to
+ * 128 go on the MMA's N), else 0. */
+int bwg_grouped_swap_rows(int m0, int row_end, int tile_m);
+
 /* Library version string. */
 const char* bwg_version(void);
 

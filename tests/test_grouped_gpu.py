@@ -101,3 +101,25 @@ def test_grouped_fc1_method_workload_sampled():
         J = cols[: len(rows)]
         Dref, S = oracle.gemm_elements(Abits, wl.bits(c.Bs[gi]), I, J)
         assert_within_bound(D[I, J], Dref, S, "expert %d" % gi)
+
+
+@pytest.mark.parametrize("counts", [[300, 0, 256, 1, 0, 511, 37], [16, 128, 129, 384, 100, 5]])
+def test_grouped_swapped_group_ends_exact(counts, monkeypatch):
+    """Group ends of at most 128 rows are computed with swapped operands
+    (rows on the MMA's N); the result must be exact on integer inputs, the
+    same as with swapping switched off, and rows outside every tile untouched."""
+    off = wl.offsets_from_counts(counts)
+    g = wl.generator(6100 + len(counts))
+    K, N = 192, 520
+    A = wl.randint_matrix(int(off[-1]), K, -2, 2, g)
+    Bs = [wl.randint_matrix(K, N, -2, 2, g) for _ in counts]
+    Dref, _ = oracle.grouped_gemm(wl.bits(A), [wl.bits(b) for b in Bs], off)
+    want = oracle.round_to(Dref, "bf16")
+    monkeypatch.setenv("BWG_GROUPED_SWAP", "1")
+    D, st, word = run_grouped(A, Bs, off)
+    assert st == 0, hex(word)
+    assert_bits_equal(D, want, "swapped ends")
+    monkeypatch.delenv("BWG_GROUPED_SWAP")
+    D2, st, word = run_grouped(A, Bs, off)
+    assert st == 0, hex(word)
+    assert_bits_equal(D2, want, "padded ends")

@@ -262,3 +262,17 @@ def test_streamk_ranges_cover_each_tile_iteration_once(ops, tiles, kb, C):
         L.bwg_streamk_tile_workers(t, kb, W, C, ctypes.byref(first), ctypes.byref(count))
         owners = sorted({i for i in range(C) for p in range(begins[i], begins[i + 1]) if t * kb <= p < (t + 1) * kb})
         assert owners == list(range(first.value, first.value + count.value))
+
+
+def test_grouped_swapped_tiles_are_the_short_group_ends(ops):
+    L = ops.lib()
+    assert L.bwg_grouped_swap_rows(1024, 1030, 256) == 6      # 6-row tail: swapped
+    assert L.bwg_grouped_swap_rows(1024, 1152, 256) == 128    # 128 rows: swapped
+    assert L.bwg_grouped_swap_rows(1024, 1153, 256) == 0      # 129 rows: padded tile
+    assert L.bwg_grouped_swap_rows(0, 2048, 256) == 0         # full tile
+    assert L.bwg_grouped_swap_rows(0, 37, 256) == 37          # whole small group
+    # the expert counts of the FC1 workload: which tails go swapped
+    from blackwell_tensor_core_gb300 import workloads as wl
+    counts = wl.expert_counts(4096, 8, 32, wl.generator(1005))
+    swapped = [c % 256 for c in counts if 0 < c % 256 <= 128]
+    assert len(swapped) == 15 and max(swapped) == 68
