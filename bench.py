@@ -36,6 +36,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 METRIC = "GEMM TFLOPS at 8192^3 BF16 (device-timed) and % of dense BF16 tensor peak"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_gemm_8192.txt")
 KERNEL_SOURCES = ["gemm_tc.cu", "ptx.cuh", "layout.h", "params.h", "api.cu"]
+KERNEL_NAMES = {2: "persistent 1-CTA", 3: "persistent CTA pair (cta_group::2)",
+                4: "swapped small-M", 5: "two pairs sharing B by TMA multicast",
+                6: "persistent CTA pair, two MMA consumers (cta_group::2)"}
 
 
 # ----------------------------------------------------------------- infra ----
@@ -440,7 +443,9 @@ def run_ours(args, rank, world, local):
         "config": {"workload": "gemm_8192x8192x8192_bf16in_fp32acc_bf16out", "M": case.M, "N": case.N,
                    "K": case.K, "inputs": "U[-1,1], seed 1003, row-major A and B",
                    "l2": "inputs larger than L2 (A+B = 256 MiB > 129 MB); no flush",
-                   "kernel": "persistent 2-CTA 256x256x64, %d stages, grid %d" % (plan.stages, plan.grid),
+                   "kernel": "%s, tile %dx%dx64, %d stages, grid %d" % (
+                       KERNEL_NAMES.get(plan.kernel, plan.kernel), plan.tile_m, plan.tile_n, plan.stages,
+                       plan.grid),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,

@@ -57,6 +57,7 @@ struct DeviceState {
   unsigned long long* err = nullptr;
   int clusters_2cta = 0;
   int clusters_mc = 0;  // 4-CTA clusters (two pairs)
+  int clusters_2c = 0;  // pairs of the two-consumer kernel
   int ctas_1cta = 0;
   int clusters_grouped = 0;
 };
@@ -146,10 +147,14 @@ int streamk_max_sharers(int tiles, int kb, int grid) {
 
 // ------------------------------------------------------------ planning -----
 
-int dense_stage_bytes(int cg) { return kRowsPerCta * kBK * 2 + (kTileN / cg) * kBK * 2; }
+// Per-CTA bytes of one ring stage: nc A blocks of 128 rows and this CTA's
+// share of the B columns, 64 K deep.
+int dense_stage_bytes(int cg, int nc = 1) {
+  return nc * kRowsPerCta * kBK * 2 + (kTileN / cg) * kBK * 2;
+}
 
-int dense_smem(int cg, int stages, bool direct_store = false) {
-  return 1024 + stages * dense_stage_bytes(cg) + (direct_store ? 0 : kEpiBytes) + kBarrierArea;
+int dense_smem(int cg, int stages, bool direct_store = false, int nc = 1) {
+  return 1024 + stages * dense_stage_bytes(cg, nc) + (direct_store ? 0 : kEpiBytes) + kBarrierArea;
 }
 
 // Epilogue choice: "tma" (staged boxes + TMA stores) or "direct" (rows stored
@@ -184,7 +189,7 @@ int no_tail_split_from_env() {
 
 bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_count, int max_smem,
                       int force_kernel, int force_stages, int max_clusters_2cta, int max_ctas_1cta,
-                      int max_clusters_mc, bwg_plan_info* o) {
+                      int max_clusters_mc, int max_clusters_2c, bwg_plan_info* o) {
   std::memset(o, 0, sizeof(*o));
   if (M == 0 || N == 0) {
     o->kernel = BWG_KERNEL_NONE;
@@ -195,9 +200,21 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     return BWG_OK;
   }
   int kind = force_kernel;
-  if (kind == 0) kind = (M <= kSmallMMaxM) ? BWG_KERNEL_SMALL_M : BWG_KERNEL_2CTA;
+  if (kind == 0) {
+    // 512x256 tiles (two MMA consumers per pair) need 25% fewer shared-memory
+    // bytes per FLOP than 256x256 ones, which is what limits these kernels;
+    // use them while they still give every pair at least one tile.
+    const int pairs = max_clusters_2c > 0 ? max_clusters_2c : sm_count / 2;
+    const long long tiles_2c = static_cast<long long>(ceil_div(M, 4 * kRowsPerCta)) * ceil_div(N, kTileN);
+    if (M <= kSmallMMaxM)
+      kind = BWG_KERNEL_SMALL_M;
+    else if (tiles_2c >= pairs)
+      kind = BWG_KERNEL_2CTA_2C;
+    else
+      kind = BWG_KERNEL_2CTA;
+  }
   if (kind != BWG_KERNEL_1CTA && kind != BWG_KERNEL_2CTA && kind != BWG_KERNEL_SMALL_M &&
-      kind != BWG_KERNEL_2CTA_MC)
+      kind != BWG_KERNEL_2CTA_MC && kind != BWG_KERNEL_2CTA_2C)
     return BWG_ERR_INVALID_ARG;
   if (kind == BWG_KERNEL_SMALL_M && M > kSmallMMaxM) return BWG_ERR_UNSUPPORTED;
   const uint32_t fmt = fp16_in ? kFmtF16 : kFmtBF16;
@@ -240,20 +257,23 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
   } else {
     const int cg = (kind == BWG_KERNEL_1CTA) ? 1 : 2;
     const int mc = (kind == BWG_KERNEL_2CTA_MC) ? 2 : 1;  // pairs per cluster
+    const int nc = (kind == BWG_KERNEL_2CTA_2C) ? 2 : 1;  // MMA consumers per pair
     const bool direct = direct_store_from_env();
-    o->tile_m = kRowsPerCta * cg;
+    o->tile_m = kRowsPerCta * cg * nc;
     o->tile_n = kTileN;
     o->mma_m = kRowsPerCta * cg;
     o->mma_n = kTileN;
-    const int fixed = dense_smem(cg, 0, direct);
-    int stages = std::min(8, (max_smem - fixed) / dense_stage_bytes(cg));
+    const int fixed = dense_smem(cg, 0, direct, nc);
+    int stages = std::min(8, (max_smem - fixed) / dense_stage_bytes(cg, nc));
     if (force_stages > 0) stages = force_stages;
-    if (stages < 2 || dense_smem(cg, stages, direct) > max_smem) return BWG_ERR_UNSUPPORTED;
+    if (stages < 2 || dense_smem(cg, stages, direct, nc) > max_smem) return BWG_ERR_UNSUPPORTED;
     o->stages = stages;
     o->tiles = ceil_div(M, o->tile_m) * ceil_div(N, o->tile_n);
-    o->smem_input_per_cta = stages * dense_stage_bytes(cg);
-    o->smem_total = dense_smem(cg, stages, direct);
-    if (mc == 2) {
+    o->smem_input_per_cta = stages * dense_stage_bytes(cg, nc);
+    o->smem_total = dense_smem(cg, stages, direct, nc);
+    if (nc == 2) {
+      o->grid = 2 * std::min(o->tiles, max_clusters_2c > 0 ? max_clusters_2c : sm_count / 2);
+    } else if (mc == 2) {
       // schedule units are stacks of two pair tiles; 4-CTA clusters
       const int units = ceil_div(ceil_div(M, o->tile_m), 2) * ceil_div(N, o->tile_n);
       o->grid = 4 * std::min(units, max_clusters_mc > 0 ? max_clusters_mc : sm_count / 4);
@@ -262,7 +282,7 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     } else {
       o->grid = std::min(o->tiles, max_ctas_1cta > 0 ? max_ctas_1cta : sm_count);
     }
-    o->tx_bytes = static_cast<uint32_t>(cg * dense_stage_bytes(cg));
+    o->tx_bytes = static_cast<uint32_t>(cg * dense_stage_bytes(cg, nc));
     o->idesc = make_idesc_f16(fmt, /*a_mn_major=*/false, /*b_mn_major=*/true, o->mma_m, kTileN);
   }
   o->coverage = static_cast<double>(M) * N / (static_cast<double>(o->tiles) * o->tile_m * o->tile_n);
@@ -270,7 +290,7 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
   if (kind != BWG_KERNEL_SMALL_M) {
     const int per_unit = kind == BWG_KERNEL_2CTA_MC ? 2 : 1;
     const int base_units = ceil_div(ceil_div(M, o->tile_m), per_unit) * ceil_div(N, o->tile_n);
-    const int workers = kind == BWG_KERNEL_2CTA ? o->grid / 2
+    const int workers = (kind == BWG_KERNEL_2CTA || kind == BWG_KERNEL_2CTA_2C) ? o->grid / 2
                         : kind == BWG_KERNEL_2CTA_MC ? o->grid / 4 : o->grid;
     o->units = base_units + (no_tail_split_from_env() ? 0 : tail_split_count(base_units, workers));
   }
@@ -352,10 +372,12 @@ bwg_status ensure_device(DeviceState** out) {
       } else {
         st.clusters_2cta = max_active_clusters_gemm(2, false, dense_smem(2, 6));
         st.clusters_mc = max_active_clusters_gemm(4, false, dense_smem(2, 6));
+        st.clusters_2c = max_active_clusters_gemm_2c(dense_smem(2, 4, false, 2));
         st.clusters_grouped = max_active_clusters_gemm(2, true, dense_smem(2, 6));
         st.ctas_1cta = max_active_clusters_gemm(1, false, dense_smem(1, 4));
         if (st.clusters_2cta <= 0) st.clusters_2cta = st.sm_count / 2;
         if (st.clusters_mc <= 0) st.clusters_mc = st.sm_count / 4;
+        if (st.clusters_2c <= 0) st.clusters_2c = st.sm_count / 2;
         if (st.clusters_grouped <= 0) st.clusters_grouped = st.sm_count / 2;
         if (st.ctas_1cta <= 0) st.ctas_1cta = st.sm_count;
       }
@@ -408,6 +430,7 @@ int force_kernel_from_env() {
   if (!std::strcmp(v, "1cta")) return BWG_KERNEL_1CTA;
   if (!std::strcmp(v, "2cta")) return BWG_KERNEL_2CTA;
   if (!std::strcmp(v, "2cta_mc")) return BWG_KERNEL_2CTA_MC;
+  if (!std::strcmp(v, "2cta_2c")) return BWG_KERNEL_2CTA_2C;
   if (!std::strcmp(v, "small_m")) return BWG_KERNEL_SMALL_M;
   return 0;
 }
@@ -438,7 +461,8 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
   if ((s = ensure_device(&st)) != BWG_OK) return s;
   bwg_plan_info pl;
   s = plan_dense(M, N, K, out_dtype, fp16_in, st->sm_count, st->max_smem, force_kernel_from_env(),
-                 force_stages_from_env(), st->clusters_2cta, st->ctas_1cta, st->clusters_mc, &pl);
+                 force_stages_from_env(), st->clusters_2cta, st->ctas_1cta, st->clusters_mc,
+                 st->clusters_2c, &pl);
   if (s != BWG_OK) return s;
   if (pl.kernel == BWG_KERNEL_ZERO)
     return launch_status(launch_zero_fill(D, M, N, ldd, out_elt(out_dtype), stream));
@@ -515,6 +539,8 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
     return launch_status(launch_gemm_2cta(p, pl.grid, pl.smem_total, stream));
   if (pl.kernel == BWG_KERNEL_2CTA_MC)
     return launch_status(launch_gemm_2cta_mc(p, pl.grid, pl.smem_total, stream));
+  if (pl.kernel == BWG_KERNEL_2CTA_2C)
+    return launch_status(launch_gemm_2cta_2c(p, pl.grid, pl.smem_total, stream));
   return launch_status(launch_gemm_1cta(p, pl.grid, pl.smem_total, stream));
 }
 
@@ -660,7 +686,7 @@ bwg_status run_small_m_noalloc(const void* A, const void* B, void* D, int M, int
   if (K == 0) return launch_status(launch_zero_fill(D, M, N, ldd, out_elt(out_dtype), stream));
   bwg_plan_info pl;
   s = plan_dense(M, N, K, out_dtype, false, st->sm_count, st->max_smem, BWG_KERNEL_SMALL_M, 0,
-                 st->clusters_2cta, st->ctas_1cta, st->clusters_mc, &pl);
+                 st->clusters_2cta, st->ctas_1cta, st->clusters_mc, st->clusters_2c, &pl);
   if (s != BWG_OK) return s;
   // Always the stream-K form: every CTA gets at least one k-block.
   const long long iters = static_cast<long long>(pl.tiles) * pl.k_blocks;
@@ -809,7 +835,7 @@ bwg_status bwg_plan(int M, int N, int K, int out_dtype, int sm_count, int force_
     return BWG_ERR_INVALID_ARG;
   // 227 KiB of opt-in shared memory per block on sm_100-family parts.
   return plan_dense(M, N, K, out_dtype, false, sm_count, 232448, force_kernel, force_stages, 0, 0, 0,
-                    out);
+                    0, out);
 }
 
 bwg_status bwg_check_gemm_args(const void* A, const void* B, const void* D, int M, int N, int K,

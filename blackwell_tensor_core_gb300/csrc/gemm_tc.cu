@@ -64,9 +64,9 @@ struct Tile {
 // MC pairs per cluster (1, or 2 when the pairs share B through TMA multicast):
 // a schedule unit is then a stack of MC tiles along M with the same columns,
 // and pair `pair` of the cluster takes tile row (unit row * MC + pair).
-template <int CG, int MC, bool GROUPED>
+template <int CG, int MC, bool GROUPED, int NC = 1>
 struct Sched {
-  static constexpr int kTileM = kRowsPerCta * CG;
+  static constexpr int kTileM = kRowsPerCta * CG * NC;
   const GemmParams& p;
   const int* prefix;  // grouped tables in shared memory: prefix[G+1], lo[G], hi[G]
   const int* lo;
@@ -132,7 +132,9 @@ __device__ __forceinline__ const CUtensorMap* b_map(const PT& P, int g) {
     return &P.map_b;
 }
 
-template <int CG, int MC, bool GROUPED, class PT>
+// NC = MMA consumers per pair (1, or 2 for 512x256 tiles: two A blocks per
+// stage share one B stage, each consumer owning half of the TMEM columns).
+template <int CG, int MC, bool GROUPED, int NC, class PT>
 __device__ void gemm_body(const PT& P, const GemmParams& p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -145,9 +147,12 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
   const int S = p.stages;
   constexpr uint32_t kBCols = kTileN / CG;             // B columns a CTA loads for a whole tile
   constexpr uint32_t kBStageBytes = kBCols * kBK * 2;  // 32 KiB (1 CTA) or 16 KiB (pair)
+  constexpr uint32_t kAStage = NC * kAStageBytes;      // one 128-row A block per consumer
+  constexpr uint32_t kEpiWarp0 = NC == 1 ? 2u : 4u;    // first epilogue warp
+  constexpr uint32_t kEpiBufs = NC == 1 ? 2u : 1u;     // staging boxes per epilogue warp
 
   const uint32_t smem_a = base;
-  const uint32_t smem_b = smem_a + S * kAStageBytes;
+  const uint32_t smem_b = smem_a + S * kAStage;
   const uint32_t smem_epi = smem_b + S * kBStageBytes;
   const uint32_t smem_bar = smem_epi + (p.direct_store ? 0u : static_cast<uint32_t>(kEpiBytes));
   auto full_bar = [&](int s) { return smem_bar + 8u * s; };
@@ -161,7 +166,8 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), MC);  // one MMA commit per pair (multicast writes need both)
+      // one MMA commit per pair and consumer (multicast writes need every pair)
+      mbar_init(empty_bar(s), MC * NC);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(acc_full_bar(a), 1);
@@ -200,7 +206,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
 
   const int first = static_cast<int>((CG == 2) ? cluster_id_x() : blockIdx.x);
   const int stride = static_cast<int>((CG == 2) ? num_clusters_x() : gridDim.x);
-  const Sched<CG, MC, GROUPED> sched(p, t_prefix, t_lo, t_hi, stride, static_cast<int>(pair));
+  const Sched<CG, MC, GROUPED, NC> sched(p, t_prefix, t_lo, t_hi, stride, static_cast<int>(pair));
   const int total = sched.total();
   bool aborted = false;
 
@@ -219,7 +225,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         // (the whole 128-row box is loaded: fewer, larger requests measured
         // faster than fetching only the rows used)
         const uint32_t half_rows = static_cast<uint32_t>(((tl.swap_rows + 15) & ~15) / 2);
-        const uint32_t stage_tx = CG * (kAStageBytes + b_cols * kBK * 2) + p.tx_extra;
+        const uint32_t stage_tx = CG * (kAStage + b_cols * kBK * 2) + p.tx_extra;
         const int a_row = tl.swap_rows > 0 ? tl.m0 + static_cast<int>(rank * half_rows)
                                            : tl.m0 + static_cast<int>(rank) * kRowsPerCta;
         const int b_col = tl.n0 + static_cast<int>(rank * b_cols);
@@ -230,13 +236,15 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
             aborted = true;
             break;
           }
-          const uint32_t sa = smem_a + s * kAStageBytes;
+          const uint32_t sa = smem_a + s * kAStage;
           const uint32_t sb = smem_b + s * kBStageBytes;
           const int k0 = kb * kBK;
           if constexpr (CG == 2) {
             if (rank == 0) mbar_arrive_expect_tx(full_bar(s), stage_tx);
             const uint32_t fb = mapa_shared(full_bar(s), leader);
-            tma_load_2d_pair(sa, &p.map_a, fb, k0, a_row);
+#pragma unroll
+            for (int c = 0; c < NC; ++c)  // consumer c's rows start 256 rows further
+              tma_load_2d_pair(sa + c * kAStageBytes, &p.map_a, fb, k0, a_row + c * 2 * kRowsPerCta);
             if constexpr (MC == 1) {
               for (uint32_t j = 0; j < b_chunks; ++j)
                 tma_load_2d_pair(sb + j * kBChunkBytes, mb, fb, b_col + 64 * j, k0);
@@ -262,17 +270,20 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp >= 1 && warp <= static_cast<uint32_t>(NC)) {
     // ---- MMA issuer: one thread of CTA 0 drives the tensor cores -----------
+    // With two consumers, warp 1 + c issues consumer c's MMAs (its A block,
+    // the shared B stage) into TMEM columns [256c, 256c + 256).
     // Commit masks: the stage-empty signal must reach every CTA whose shared
     // memory the next loads of that stage write (all pairs when B is
     // multicast); the accumulator-full signal only this pair.
     const uint16_t empty_mask = static_cast<uint16_t>(MC == 2 ? 0xF : 0x3);
     const uint16_t acc_mask = static_cast<uint16_t>(0x3u << (2 * pair));
+    const int cons = static_cast<int>(warp) - 1;  // consumer of this warp
     if (rank == 0 && lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      int acc = 0;
+      int acc = NC == 1 ? 0 : cons;  // accumulator slot: alternating, or the consumer's own
       uint32_t acc_ph = 0;
       for (int t = first; t < total && !aborted; t += stride) {
         const Tile tl = sched.at(t);
@@ -297,7 +308,8 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
             break;
           }
           tc_fence_after();
-          const uint64_t a_desc = make_smem_desc(smem_a + s * kAStageBytes, 16, 1024, kSwizzle128B);
+          const uint64_t a_desc =
+              make_smem_desc(smem_a + s * kAStage + cons * kAStageBytes, 16, 1024, kSwizzle128B);
           const uint64_t b_desc =
               make_smem_desc(smem_b + s * kBStageBytes, kBChunkBytes, 1024, kSwizzle128B);
 #pragma unroll
@@ -322,22 +334,27 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
           mma_commit_pair_mc(acc_full_bar(acc), acc_mask);
         else
           mma_commit_1cta(acc_full_bar(acc));
-        if (++acc == 2) {
-          acc = 0;
+        if constexpr (NC == 1) {
+          if (++acc == 2) {
+            acc = 0;
+            acc_ph ^= 1u;
+          }
+        } else {
           acc_ph ^= 1u;
         }
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp >= kEpiWarp0) {
     // ---- epilogue: TMEM -> registers -> convert -> swizzled SMEM -> TMA -----
     const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may read
-    const uint32_t ebuf = smem_epi + (warp - 2u) * 2u * kEpiBufBytes;
+    const int cons = NC == 1 ? 0 : static_cast<int>((warp - kEpiWarp0) >> 2);  // accumulator owner
+    const uint32_t ebuf = smem_epi + (warp - kEpiWarp0) * kEpiBufs * kEpiBufBytes;
     const uint32_t acc_empty_leader0 =
         (CG == 2) ? mapa_shared(acc_empty_bar(0), leader) : acc_empty_bar(0);
     const bool out32 = p.out_dtype == kOutF32;
     const bool outbf = p.out_dtype == kOutBF16;
-    int acc = 0;
+    int acc = NC == 1 ? 0 : cons;
     uint32_t acc_ph = 0;
     uint32_t buf = 0;
     for (int t = first; t < total; t += stride) {
@@ -349,7 +366,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         break;
       }
       tc_fence_after();
-      const int row_w = tl.m0 + static_cast<int>(rank * kRowsPerCta + q * 32u);
+      const int row_w = tl.m0 + cons * 2 * kRowsPerCta + static_cast<int>(rank * kRowsPerCta + q * 32u);
       const uint32_t t_acc = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc) * kTileN;
       if (GROUPED && tl.swap_rows > 0) {
         // Swapped tile: TMEM lane = output column, TMEM column = row.  Each
@@ -419,7 +436,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         if (col0 >= p.N) continue;
         const bool whole_box = !p.direct_store && (!GROUPED || (row_w + 32 <= tl.row_end));
         if (whole_box) {
-          if (lane == 0) bulk_wait_group_read<1>();
+          if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
           __syncwarp();
           const uint32_t sb = ebuf + buf * kEpiBufBytes;
 #pragma unroll
@@ -432,7 +449,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
             tma_store_2d(&p.map_d, sb, col0, row_w);
             bulk_commit_group();
           }
-          buf ^= 1u;
+          buf = (buf + 1u) % kEpiBufs;
         } else {
           // Ragged end of a group, or the register-store epilogue: each
           // thread stores its own row (64 or 32 columns), if inside.
@@ -461,8 +478,12 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
           }
         }
       }
-      if (++acc == 2) {
-        acc = 0;
+      if constexpr (NC == 1) {
+        if (++acc == 2) {
+          acc = 0;
+          acc_ph ^= 1u;
+        }
+      } else {
         acc_ph ^= 1u;
       }
     }
@@ -490,19 +511,27 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
 
 template <int CG, int MC>
 __global__ void __launch_bounds__(kThreads, 1) gemm_dense_kernel(const __grid_constant__ GemmParams p) {
-  gemm_body<CG, MC, false>(p, p);
+  gemm_body<CG, MC, false, 1>(p, p);
+}
+
+// 512x256 tiles on a pair: warp 0 TMA, warps 1-2 MMA (one per consumer),
+// warp 3 idle, warps 4-7 and 8-11 the epilogue of consumer 0 and 1.
+__global__ void __launch_bounds__(kThreads2C, 1)
+    gemm_dense_2c_kernel(const __grid_constant__ GemmParams p) {
+  gemm_body<2, 1, false, 2>(p, p);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_grouped_kernel(const __grid_constant__ GroupedParams p) {
-  gemm_body<2, 1, true>(p, p.base);
+  gemm_body<2, 1, true, 1>(p, p.base);
 }
 
 template <class K, class P>
-cudaError_t launch_cluster(K kernel, const P& p, int cg, int grid, size_t smem, cudaStream_t s) {
+cudaError_t launch_cluster(K kernel, const P& p, int cg, int grid, size_t smem, cudaStream_t s,
+                           int threads = kThreads) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -529,14 +558,18 @@ cudaError_t launch_gemm_2cta_mc(const GemmParams& p, int grid, size_t smem, cuda
   return launch_cluster(gemm_dense_kernel<2, 2>, p, 4, grid, smem, s);
 }
 
+cudaError_t launch_gemm_2cta_2c(const GemmParams& p, int grid, size_t smem, cudaStream_t s) {
+  return launch_cluster(gemm_dense_2c_kernel, p, 2, grid, smem, s, kThreads2C);
+}
+
 cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, cudaStream_t s) {
   return launch_cluster(gemm_grouped_kernel, p, 2, grid, smem, s);
 }
 
-static int occupancy_clusters(const void* fn, int cg, size_t smem) {
+static int occupancy_clusters(const void* fn, int cg, size_t smem, int threads = kThreads) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(cg), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -553,6 +586,10 @@ static int occupancy_clusters(const void* fn, int cg, size_t smem) {
   return n;
 }
 
+int max_active_clusters_gemm_2c(size_t smem) {
+  return occupancy_clusters(reinterpret_cast<const void*>(gemm_dense_2c_kernel), 2, smem, kThreads2C);
+}
+
 int max_active_clusters_gemm(int cluster, bool grouped, size_t smem) {
   const void* fn = grouped ? reinterpret_cast<const void*>(gemm_grouped_kernel)
                    : cluster == 4 ? reinterpret_cast<const void*>(gemm_dense_kernel<2, 2>)
@@ -562,9 +599,10 @@ int max_active_clusters_gemm(int cluster, bool grouped, size_t smem) {
 }
 
 cudaError_t set_gemm_attributes(size_t smem) {
-  const void* fns[4] = {reinterpret_cast<const void*>(gemm_dense_kernel<1, 1>),
+  const void* fns[5] = {reinterpret_cast<const void*>(gemm_dense_kernel<1, 1>),
                         reinterpret_cast<const void*>(gemm_dense_kernel<2, 1>),
                         reinterpret_cast<const void*>(gemm_dense_kernel<2, 2>),
+                        reinterpret_cast<const void*>(gemm_dense_2c_kernel),
                         reinterpret_cast<const void*>(gemm_grouped_kernel)};
   for (const void* fn : fns) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,

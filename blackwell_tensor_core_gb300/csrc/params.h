@@ -9,6 +9,7 @@
 namespace bwg {
 
 constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kThreads2C = 384;      // two-consumer pair kernel: 12 warps
 constexpr int kBK = 64;              // K per stage: one 128-byte swizzle row of 16-bit data
 constexpr int kTileN = 256;          // output columns per tile (MMA N)
 constexpr int kRowsPerCta = 128;     // accumulator rows per CTA (TMEM lanes)
@@ -80,6 +81,8 @@ struct SmallMParams {
 cudaError_t launch_gemm_1cta(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_gemm_2cta(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_gemm_2cta_mc(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_gemm_2cta_2c(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
+int max_active_clusters_gemm_2c(size_t smem);
 cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_small_m(const SmallMParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_zero_fill(void* d, int rows, int cols, int ld, int elt_bytes, cudaStream_t s);

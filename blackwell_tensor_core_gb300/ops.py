@@ -22,7 +22,7 @@ OUT_FP32 = 1
 OUT_FP16 = 2
 _OUT_CODES = {torch.bfloat16: OUT_BF16, torch.float32: OUT_FP32, torch.float16: OUT_FP16}
 
-KERNEL_NONE, KERNEL_ZERO, KERNEL_1CTA, KERNEL_2CTA, KERNEL_SMALL_M, KERNEL_2CTA_MC = range(6)
+KERNEL_NONE, KERNEL_ZERO, KERNEL_1CTA, KERNEL_2CTA, KERNEL_SMALL_M, KERNEL_2CTA_MC, KERNEL_2CTA_2C = range(7)
 
 STATUS_NAMES = {0: "BWG_OK", 1: "BWG_ERR_INVALID_ARG", 2: "BWG_ERR_ALIGNMENT",
                 3: "BWG_ERR_UNSUPPORTED", 4: "BWG_ERR_CUDA", 5: "BWG_ERR_TIMEOUT"}

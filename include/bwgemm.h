@@ -167,7 +167,8 @@ typedef enum {
   BWG_KERNEL_1CTA = 2,     /* 128 x 256 tiles, one CTA each */
   BWG_KERNEL_2CTA = 3,     /* 256 x 256 tiles on CTA pairs (cta_group::2) */
   BWG_KERNEL_SMALL_M = 4,  /* swapped operands, MMA N = M rounded up to 16 */
-  BWG_KERNEL_2CTA_MC = 5   /* two pairs per 4-CTA cluster, B shared by TMA multicast */
+  BWG_KERNEL_2CTA_MC = 5,  /* two pairs per 4-CTA cluster, B shared by TMA multicast */
+  BWG_KERNEL_2CTA_2C = 6   /* 512 x 256 tiles on a pair: two MMA consumers share each B stage */
 } bwg_kernel_kind;
 
 typedef struct {

@@ -300,3 +300,29 @@ def test_small_m_tile_stride(tile_n, out, monkeypatch):
     else:
         assert_bits_equal(D, oracle.round_to(Dref, "bf16"), "tile_n %d" % tile_n)
     assert torch.all(full[:, 1000:] == 5.0)
+
+
+@pytest.mark.parametrize("shape", [(512, 256, 512), (520, 600, 456), (1000, 136, 1000), (1536, 2304, 640),
+                                   (129, 264, 72)])
+def test_two_consumer_kernel_exact(shape):
+    """512x256 tiles on a pair with two MMA consumers sharing each B stage:
+    exact on integer inputs, including ragged M (second consumer's rows
+    partly or wholly outside), ragged N and K, and the last-wave split."""
+    M, N, K = shape
+    g = wl.generator(5900 + M + N)
+    A = wl.randint_matrix(M, K, -2, 2, g)
+    B = wl.randint_matrix(K, N, -2, 2, g)
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+    D, _ = gpu_gemm(A, B, wl.OUT_FP32, "2cta_2c")
+    assert np.array_equal(D.double().numpy(), Dref)
+    D16, _ = gpu_gemm(A, B, wl.OUT_BF16, "2cta_2c")
+    assert_bits_equal(D16, oracle.round_to(Dref, "bf16"), "two consumers bf16")
+
+
+def test_two_consumer_kernel_at_8192_sampled():
+    c = wl.large_case()
+    D, _ = gpu_gemm(c.A, c.B, c.out_dtype, "2cta_2c")
+    _check_sampled(c.A, c.B, D, 8000, 15, c.name + " two consumers")
+    for r in (255, 256, 511, 512):
+        Dref, S = oracle.gemm(wl.bits(c.A[r:r + 1]), wl.bits(c.B))
+        assert_within_bound(D[r:r + 1], Dref, S, "row %d" % r)

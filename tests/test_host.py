@@ -101,8 +101,9 @@ def test_planner_stage_and_barrier_accounting(ops):
 
 def test_planner_choices(ops):
     big = ops.plan(8192, 8192, 8192)
-    assert big.kernel == ops.KERNEL_2CTA and big.stages == 6 and big.tiles == 1024
-    assert big.grid == 152 and big.smem_total <= 232448
+    assert big.kernel == ops.KERNEL_2CTA_2C and big.stages == 4 and big.tiles == 512
+    assert big.tile_m == 512 and big.grid == 152 and big.smem_total <= 232448
+    assert ops.plan(2048, 2048, 2048).kernel == ops.KERNEL_2CTA  # 32 big tiles < 76 pairs
     small = ops.plan(72, 16384, 7168)
     assert small.kernel == ops.KERNEL_SMALL_M and small.mma_n == 80
     # whole 128-column tiles walking K in step; stream-K for few or too many tiles
@@ -115,6 +116,9 @@ def test_planner_choices(ops):
     assert ops.plan(0, 10, 10).kernel == ops.KERNEL_NONE
     assert ops.plan(10, 10, 0).kernel == ops.KERNEL_ZERO
     assert ops.plan(129, 10, 10).kernel == ops.KERNEL_2CTA
+    p2 = ops.plan(512, 512, 512, force_kernel=ops.KERNEL_2CTA_2C, force_stages=2)
+    assert p2.smem_input_per_cta // 2 == 48 * 1024  # two A blocks + one B block per CTA per stage
+    assert p2.tx_bytes == 2 * 48 * 1024
     assert ops.plan(128, 10, 10).kernel == ops.KERNEL_SMALL_M
 
 
@@ -241,10 +245,12 @@ def test_last_wave_split_covers_every_column_once(ops, T, C):
 
 
 def test_plan_reports_split_units(ops):
-    big = ops.plan(8192, 8192, 8192)
+    big = ops.plan(8192, 8192, 8192, force_kernel=ops.KERNEL_2CTA)
     assert big.tiles == 1024 and big.units == 1024 + 1024 % 76
-    mid = ops.plan(4096, 4096, 4096)
+    mid = ops.plan(4096, 4096, 4096, force_kernel=ops.KERNEL_2CTA)
     assert mid.units == 256 + 256 % 76
+    two = ops.plan(8192, 8192, 8192)
+    assert two.tiles == 512 and two.units == 512  # remainder 56 > 38: no split
 
 
 @pytest.mark.parametrize("tiles,kb,C", [(128, 112, 152), (128, 112, 128), (3, 1, 152), (1, 200, 152),

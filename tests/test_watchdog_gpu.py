@@ -22,7 +22,8 @@ def _built():
     build.build()
 
 
-@pytest.mark.parametrize("kind,M", [("2cta", 256), ("1cta", 256), ("2cta_mc", 512), (None, 64)])
+@pytest.mark.parametrize("kind,M", [("2cta", 256), ("1cta", 256), ("2cta_mc", 512), ("2cta_2c", 512),
+                                    (None, 64)])
 def test_stalled_stage_barrier_times_out_and_context_survives(kind, M):
     from blackwell_tensor_core_gb300 import ops
     from gpu_util import forced_kernel
