@@ -292,7 +292,13 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     const int base_units = ceil_div(ceil_div(M, o->tile_m), per_unit) * ceil_div(N, o->tile_n);
     const int workers = (kind == BWG_KERNEL_2CTA || kind == BWG_KERNEL_2CTA_2C) ? o->grid / 2
                         : kind == BWG_KERNEL_2CTA_MC ? o->grid / 4 : o->grid;
-    o->units = base_units + (no_tail_split_from_env() ? 0 : tail_split_count(base_units, workers));
+    int f = 1;
+    const bool two = kind == BWG_KERNEL_2CTA_2C;
+    const int R = no_tail_split_from_env()
+                      ? 0
+                      : tail_split(base_units, workers, two ? 4 : 2, two ? kCostHalf2 : kCostHalf1,
+                                   kCostQuarter2, &f);
+    o->units = base_units - R + R * f;
   }
   return BWG_OK;
 }
@@ -871,6 +877,14 @@ void bwg_grouped_tile(int t, int G, const int* prefix, const int* lo, const int*
 }
 
 int bwg_tail_split(int T, int C) { return tail_split_count(T, C); }
+
+int bwg_tail_split_f(int T, int C, int max_f, int* f) {
+  return tail_split(T, C, max_f, max_f == 4 ? kCostHalf2 : kCostHalf1, kCostQuarter2, f);
+}
+
+void bwg_unit_part(int u, int T, int R, int f, int* tile, int* part, int* parts) {
+  unit_part(u, T, R, f, tile, part, parts);
+}
 
 void bwg_unit_tile(int u, int T, int R, int tile_n, int* tile, int* col_off, int* width) {
   unit_tile(u, T, R, tile_n, tile, col_off, width);

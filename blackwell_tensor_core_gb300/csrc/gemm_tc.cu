@@ -59,6 +59,7 @@ struct Tile {
   int row_end;
   int g;
   int swap_rows;  // > 0: rows m0 .. m0+swap_rows-1 computed with swapped operands
+  int cmask;      // MMA consumers with work in this unit (bit c: rows m0 + 256c ..)
 };
 
 // MC pairs per cluster (1, or 2 when the pairs share B through TMA multicast):
@@ -73,8 +74,9 @@ struct Sched {
   const int* hi;
   int pair;           // this CTA's pair inside the cluster
   int rows_of_units;  // unit rows (tile rows / MC, rounded up)
-  int tiles;          // whole units
-  int split;          // units of the last wave split in two along N
+  int tiles;          // whole tiles
+  int split;          // tiles of the last wave that are cut
+  int f;              // parts per cut tile (2 halves, or 4 quarters with two consumers)
 
   __device__ Sched(const GemmParams& p_, const int* prefix_, const int* lo_, const int* hi_,
                    int workers, int pair_)
@@ -84,15 +86,20 @@ struct Sched {
       tiles = prefix[p.G];
     else
       tiles = rows_of_units * p.num_n_tiles;
-    split = p.no_tail_split ? 0 : tail_split_count(tiles, workers);
+    f = 1;
+    split = p.no_tail_split ? 0
+                            : tail_split(tiles, workers, NC == 2 ? 4 : 2,
+                                         NC == 2 ? kCostHalf2 : kCostHalf1, kCostQuarter2, &f);
   }
 
-  __device__ int total() const { return tiles + split; }
+  __device__ int total() const { return tiles - split + split * f; }
 
   __device__ Tile at(int u) const {
     Tile tl;
-    int t, col_off;
-    unit_tile(u, tiles, split, kTileN, &t, &col_off, &tl.width);
+    int t, part, parts;
+    unit_part(u, tiles, split, f, &t, &part, &parts);
+    int col_off = parts == 1 ? 0 : (part & 1) * (kTileN / 2);
+    tl.width = parts == 1 ? kTileN : kTileN / 2;
     tl.swap_rows = 0;
     if constexpr (GROUPED) {
       grouped_tile(t, p.G, prefix, lo, hi, kTileM, kTileN, &tl.g, &tl.m0, &tl.n0, &tl.row_end);
@@ -113,6 +120,21 @@ struct Sched {
       tl.g = 0;
     }
     tl.n0 += col_off;
+    tl.cmask = 1;
+    if constexpr (NC == 2) {
+      // the second consumer's 256 rows start 256 rows down; skip them if
+      // they lie wholly past the end
+      tl.cmask = (tl.m0 + kRowsPerCta * CG < tl.row_end) ? 3 : 1;
+      if (parts == 4) {  // quarter: one row block, one column half, one consumer
+        if (part >> 1) {
+          tl.m0 += 2 * kRowsPerCta;
+          tl.cmask = (tl.cmask & 2) ? 1 : 0;
+        } else {
+          tl.cmask &= 1;
+        }
+      }
+      if (tl.cmask == 0) tl.width = 0;
+    }
     return tl;
   }
 };
@@ -225,7 +247,9 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         // (the whole 128-row box is loaded: fewer, larger requests measured
         // faster than fetching only the rows used)
         const uint32_t half_rows = static_cast<uint32_t>(((tl.swap_rows + 15) & ~15) / 2);
-        const uint32_t stage_tx = CG * (kAStage + b_cols * kBK * 2) + p.tx_extra;
+        const uint32_t stage_tx =
+            CG * (static_cast<uint32_t>(__popc(tl.cmask)) * kAStageBytes + b_cols * kBK * 2) +
+            p.tx_extra;
         const int a_row = tl.swap_rows > 0 ? tl.m0 + static_cast<int>(rank * half_rows)
                                            : tl.m0 + static_cast<int>(rank) * kRowsPerCta;
         const int b_col = tl.n0 + static_cast<int>(rank * b_cols);
@@ -244,7 +268,8 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
             const uint32_t fb = mapa_shared(full_bar(s), leader);
 #pragma unroll
             for (int c = 0; c < NC; ++c)  // consumer c's rows start 256 rows further
-              tma_load_2d_pair(sa + c * kAStageBytes, &p.map_a, fb, k0, a_row + c * 2 * kRowsPerCta);
+              if ((tl.cmask >> c) & 1)
+                tma_load_2d_pair(sa + c * kAStageBytes, &p.map_a, fb, k0, a_row + c * 2 * kRowsPerCta);
             if constexpr (MC == 1) {
               for (uint32_t j = 0; j < b_chunks; ++j)
                 tma_load_2d_pair(sb + j * kBChunkBytes, mb, fb, b_col + 64 * j, k0);
@@ -288,6 +313,27 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
       for (int t = first; t < total && !aborted; t += stride) {
         const Tile tl = sched.at(t);
         if (tl.width == 0) continue;
+        if (!((tl.cmask >> cons) & 1)) {
+          // No rows for this consumer: still commit once per stage (the
+          // stage-empty barrier counts every consumer), after the stage's
+          // full phase so the commit lands in the right phase.
+          for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+            if (!mbar_wait(full_bar(s), ph, p.timeout_ns)) {
+              record_fault(p.err, kFaultTimeout, kRoleMma, kBarFull, s, ph);
+              aborted = true;
+              break;
+            }
+            if constexpr (CG == 2)
+              mma_commit_pair_mc(empty_bar(s), empty_mask);
+            else
+              mma_commit_1cta(empty_bar(s));
+            if (++s == S) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+          continue;
+        }
         if (!mbar_wait(acc_empty_bar(acc), acc_ph ^ 1u, p.timeout_ns)) {
           record_fault(p.err, kFaultTimeout, kRoleMma, kBarAccEmpty, acc, acc_ph ^ 1u);
           aborted = true;
@@ -359,7 +405,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
     uint32_t buf = 0;
     for (int t = first; t < total; t += stride) {
       const Tile tl = sched.at(t);
-      if (tl.width == 0) continue;
+      if (tl.width == 0 || !((tl.cmask >> cons) & 1)) continue;
       if (!warp_wait(acc_full_bar(acc), acc_ph, p.timeout_ns)) {
         if (lane == 0) record_fault(p.err, kFaultTimeout, kRoleEpilogue, kBarAccFull, acc, acc_ph);
         aborted = true;

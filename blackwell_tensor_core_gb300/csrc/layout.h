@@ -72,32 +72,71 @@ BWG_HD void raster_tile(int t, int num_m_tiles, int num_n_tiles, int group_m, in
 }
 
 // Wave-quantisation split.  With T output tiles on C persistent workers the
-// last wave holds only R = T mod C tiles.  When R <= C/2, each of those R
-// tiles is split along N into two halves (the MMA N drops from tile_n to
-// tile_n/2 in the instruction descriptor, the MegaMoE page's dynamic N), so
-// the last wave holds 2R half tiles and lasts about half a tile.  Returns the
-// number of split tiles (0: no split); the schedule then has T + R units.
-BWG_HD int tail_split_count(int T, int C) {
+// last wave holds only R = T mod C tiles.  Each of those R tiles can be cut
+// into f parts: f = 2 halves along N (the MMA N drops to tile_n/2 in the
+// instruction descriptor, the MegaMoE page's dynamic N), or, for tiles of two
+// stacked 256-row blocks, f = 4 quarters (row block x column half).  A part is
+// not 1/f of a tile's time: these kernels are bound by how fast shared memory
+// fills, and a part loads more bytes per FLOP than a whole tile, so part f
+// costs cost_f/1000 of a tile (its stage bytes over the whole tile's).  The
+// cut that makes the last wave, ceil(f*R/C) parts long, cheapest is taken
+// (the smaller f on a tie), none if no cut beats the uncut wave.
+// Returns R (0: no cut) and the factor in *f.
+BWG_HD int tail_split(int T, int C, int max_f, int cost2, int cost4, int* f) {
+  *f = 1;
   if (C <= 0 || T <= 0) return 0;
   const int R = T % C;
-  return (R > 0 && 2 * R <= C) ? R : 0;
+  if (R == 0) return 0;
+  long long best = 1000;  // the uncut last wave: one tile-time
+  for (int cand = 2; cand <= max_f; cand *= 2) {
+    const long long waves = (static_cast<long long>(cand) * R + C - 1) / C;
+    const long long cost = waves * (cand == 2 ? cost2 : cost4);
+    if (cost < best) {
+      best = cost;
+      *f = cand;
+    }
+  }
+  return *f > 1 ? R : 0;
 }
 
-// Unit u of a schedule of T tiles whose last R tiles are split in two:
-// the tile index (in the tile order), the column offset inside the tile and
-// the unit's width in columns.
-BWG_HD void unit_tile(int u, int T, int R, int tile_n, int* tile, int* col_off, int* width) {
+// Part costs (per mille of a tile): 256x256 pair tiles cut in halves load
+// 24 of 32 KiB per stage; 512x256 two-consumer tiles load 40 (halves) or 24
+// (quarters) of 48 KiB.
+constexpr int kCostHalf1 = 750;
+constexpr int kCostHalf2 = 833;
+constexpr int kCostQuarter2 = 500;
+
+// Two-way form (halves only) for the one-consumer kernels.
+BWG_HD int tail_split_count(int T, int C) {
+  int f = 1;
+  return tail_split(T, C, 2, kCostHalf1, 0, &f);
+}
+
+// Unit u of a schedule of T tiles whose last R tiles are cut into f parts:
+// the tile index, the part (0 .. f-1, 0 for whole tiles) and the count of
+// parts of that tile (1 or f).  Whole tiles come first, then the parts of
+// each cut tile in turn.
+BWG_HD void unit_part(int u, int T, int R, int f, int* tile, int* part, int* parts) {
   const int full = T - R;
-  if (u < full) {
+  if (u < full || R == 0) {
     *tile = u;
-    *col_off = 0;
-    *width = tile_n;
+    *part = 0;
+    *parts = 1;
   } else {
     const int v = u - full;
-    *tile = full + v / 2;
-    *col_off = (v & 1) * (tile_n / 2);
-    *width = tile_n / 2;
+    *tile = full + v / f;
+    *part = v % f;
+    *parts = f;
   }
+}
+
+// Two-way form: tile index, column offset inside the tile and the unit's
+// width in columns (tile_n, or tile_n/2 for the halves).
+BWG_HD void unit_tile(int u, int T, int R, int tile_n, int* tile, int* col_off, int* width) {
+  int part = 0, parts = 1;
+  unit_part(u, T, R, 2, tile, &part, &parts);
+  *col_off = parts == 1 ? 0 : part * (tile_n / 2);
+  *width = parts == 1 ? tile_n : tile_n / 2;
 }
 
 // The instruction descriptor with its N field replaced (N a multiple of 16).

@@ -101,6 +101,10 @@ def lib() -> ctypes.CDLL:
             L.bwg_streamk_tile_workers.restype = None
             L.bwg_grouped_swap_rows.argtypes = [i, i, i]
             L.bwg_grouped_swap_rows.restype = i
+            L.bwg_tail_split_f.argtypes = [i, i, i, ip]
+            L.bwg_tail_split_f.restype = i
+            L.bwg_unit_part.argtypes = [i, i, i, i, ip, ip, ip]
+            L.bwg_unit_part.restype = None
             L.bwg_version.argtypes = []
             L.bwg_version.restype = ctypes.c_char_p
             _lib = L

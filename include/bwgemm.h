@@ -235,6 +235,17 @@ void bwg_grouped_tile(int t, int G, const int* prefix, const int* lo, const int*
  * two halves along N (0 when the remainder is more than half a wave). */
 int bwg_tail_split(int T, int C);
 
+/* General form: the cut factor f (2 halves, or 4 quarters when max_f is 4,
+ * for tiles of two 256-row blocks) that makes the last wave cheapest, where a
+ * half of a one-consumer tile costs 0.75 of a tile and a half or quarter of a
+ * two-consumer tile 0.833 or 0.5 (their shared-memory bytes per stage);
+ * returns the number of cut tiles R (0: none) and stores f. */
+int bwg_tail_split_f(int T, int C, int max_f, int* f);
+
+/* Unit u of a schedule whose last R tiles are cut into f parts: tile index,
+ * part (0 .. f-1) and parts of that tile (1 or f). */
+void bwg_unit_part(int u, int T, int R, int f, int* tile, int* part, int* parts);
+
 /* Unit u of that schedule: tile index, column offset inside the tile and
  * width in columns (tile_n, or tile_n/2 for the split tiles). */
 void bwg_unit_tile(int u, int T, int R, int tile_n, int* tile, int* col_off, int* width);

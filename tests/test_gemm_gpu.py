@@ -326,3 +326,20 @@ def test_two_consumer_kernel_at_8192_sampled():
     for r in (255, 256, 511, 512):
         Dref, S = oracle.gemm(wl.bits(c.A[r:r + 1]), wl.bits(c.B))
         assert_within_bound(D[r:r + 1], Dref, S, "row %d" % r)
+
+
+@pytest.mark.parametrize("shape", [(2048, 5120, 128), (1536, 6656, 64), (1024, 13568, 64), (1800, 5120, 72)])
+def test_two_consumer_last_wave_quarters_exact(shape, monkeypatch):
+    """Shapes whose last wave is cut into quarters (one row block and one
+    column half per unit, one MMA consumer idle) or whose second consumer
+    has no rows: exact on integers, and equal with the cut switched off."""
+    M, N, K = shape
+    g = wl.generator(6200 + M + N)
+    A = wl.randint_matrix(M, K, -2, 2, g)
+    B = wl.randint_matrix(K, N, -2, 2, g)
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+    D, _ = gpu_gemm(A, B, wl.OUT_FP32, "2cta_2c")
+    assert np.array_equal(D.double().numpy(), Dref)
+    monkeypatch.setenv("BWG_NO_TAIL_SPLIT", "1")
+    D2, _ = gpu_gemm(A, B, wl.OUT_FP32, "2cta_2c")
+    assert np.array_equal(D2.double().numpy(), Dref)

@@ -222,6 +222,7 @@ def test_grouped_schedule_flags_bad_offsets(ops):
 def test_last_wave_split_covers_every_column_once(ops, T, C):
     R = ops.lib().bwg_tail_split(T, C)
     rem = T % C
+    # halves cost 0.75 of a tile: worth it while they fit in one wave
     assert R == (rem if 0 < rem and 2 * rem <= C else 0)
     units = T + R
     tile, off, width = (ctypes.c_int() for _ in range(3))
@@ -250,7 +251,10 @@ def test_plan_reports_split_units(ops):
     mid = ops.plan(4096, 4096, 4096, force_kernel=ops.KERNEL_2CTA)
     assert mid.units == 256 + 256 % 76
     two = ops.plan(8192, 8192, 8192)
-    assert two.tiles == 512 and two.units == 512  # remainder 56 > 38: no split
+    # remainder 56 of 76: quarters (3 x 0.5) and halves (2 x 0.833) both lose to 1.0
+    assert two.tiles == 512 and two.units == 512
+    assert ops.plan(2048, 5120, 128).units == 80 - 4 + 4 * 4       # 4 left over: quarters
+    assert ops.plan(1024, 13568, 64).units == 106 - 30 + 2 * 30    # 30 left over: halves
 
 
 @pytest.mark.parametrize("tiles,kb,C", [(128, 112, 152), (128, 112, 128), (3, 1, 152), (1, 200, 152),
@@ -282,3 +286,34 @@ def test_grouped_swapped_tiles_are_the_short_group_ends(ops):
     counts = wl.expert_counts(4096, 8, 32, wl.generator(1005))
     swapped = [c % 256 for c in counts if 0 < c % 256 <= 128]
     assert len(swapped) == 15 and max(swapped) == 68
+
+
+@pytest.mark.parametrize("T,C", [(512, 76), (128, 76), (16, 76), (1024, 76), (90, 76), (3, 2), (80, 76),
+                                 (106, 76)])
+def test_quarter_split_for_two_consumer_tiles(ops, T, C):
+    L = ops.lib()
+    f = ctypes.c_int()
+    R = L.bwg_tail_split_f(T, C, 4, ctypes.byref(f))
+    rem = T % C
+    if rem == 0:
+        assert R == 0
+        return
+    # the chosen cut gives the cheapest last wave, preferring fewer parts
+    cost = {1: 1000, 2: 833, 4: 500}
+    best = min((-(-k * rem // C) * cost[k], k) for k in (1, 2, 4))
+    if best[1] == 1:
+        assert R == 0
+    else:
+        assert R == rem and f.value == best[1]
+    units = T - R + R * max(f.value, 1)
+    tile, part, parts = (ctypes.c_int() for _ in range(3))
+    seen = {}
+    for u in range(units):
+        L.bwg_unit_part(u, T, R, f.value, ctypes.byref(tile), ctypes.byref(part), ctypes.byref(parts))
+        if parts.value > 1:
+            assert u >= T - R  # parts of cut tiles come after every whole tile
+        seen.setdefault(tile.value, []).append((part.value, parts.value))
+    for t in range(T):
+        got = sorted(seen[t])
+        n = got[0][1]
+        assert got == [(k, n) for k in range(n)]
