@@ -58,6 +58,7 @@ struct DeviceState {
   int clusters_2cta = 0;
   int clusters_mc = 0;  // 4-CTA clusters (two pairs)
   int clusters_2c = 0;  // pairs of the two-consumer kernel
+  int clusters_grouped_2c = 0;
   int ctas_1cta = 0;
   int clusters_grouped = 0;
 };
@@ -379,11 +380,13 @@ bwg_status ensure_device(DeviceState** out) {
         st.clusters_2cta = max_active_clusters_gemm(2, false, dense_smem(2, 6));
         st.clusters_mc = max_active_clusters_gemm(4, false, dense_smem(2, 6));
         st.clusters_2c = max_active_clusters_gemm_2c(dense_smem(2, 4, false, 2));
+        st.clusters_grouped_2c = max_active_clusters_grouped_2c(dense_smem(2, 4, false, 2));
         st.clusters_grouped = max_active_clusters_gemm(2, true, dense_smem(2, 6));
         st.ctas_1cta = max_active_clusters_gemm(1, false, dense_smem(1, 4));
         if (st.clusters_2cta <= 0) st.clusters_2cta = st.sm_count / 2;
         if (st.clusters_mc <= 0) st.clusters_mc = st.sm_count / 4;
         if (st.clusters_2c <= 0) st.clusters_2c = st.sm_count / 2;
+        if (st.clusters_grouped_2c <= 0) st.clusters_grouped_2c = st.sm_count / 2;
         if (st.clusters_grouped <= 0) st.clusters_grouped = st.sm_count / 2;
         if (st.ctas_1cta <= 0) st.ctas_1cta = st.sm_count;
       }
@@ -571,8 +574,13 @@ bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
   if (K == 0) return launch_status(launch_zero_fill(D, M_total, N, N, 2, stream));
   const CUtensorMapDataType in_t =
       fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const int stages = force_stages_from_env() > 0 ? force_stages_from_env() : 6;
-  const int smem = dense_smem(2, stages);
+  // Two MMA consumers (512-row units) unless BWG_GROUPED_1C=1 asks for the
+  // 256-row kernel; the one-consumer kernel is also the one with swapped ends.
+  const char* one_env = std::getenv("BWG_GROUPED_1C");
+  const bool two = !(one_env != nullptr && one_env[0] == '1');
+  const int nc = two ? 2 : 1;
+  const int stages = force_stages_from_env() > 0 ? force_stages_from_env() : (two ? 4 : 6);
+  const int smem = dense_smem(2, stages, false, nc);
   if (smem > st->max_smem) return BWG_ERR_UNSUPPORTED;
   for (int g0 = 0; g0 < G; g0 += kMaxGroupsPerLaunch) {
     const int gn = std::min(kMaxGroupsPerLaunch, G - g0);
@@ -618,9 +626,11 @@ bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
     }
     // Upper bound on tiles: every group adds at most one partial row tile.
     const long long max_tiles =
-        (static_cast<long long>(ceil_div(M_total, 2 * kRowsPerCta)) + gn) * p.num_n_tiles;
-    const int clusters = static_cast<int>(std::min<long long>(max_tiles, st->clusters_grouped));
-    const cudaError_t e = launch_grouped_2cta(P, 2 * clusters, smem, stream);
+        (static_cast<long long>(ceil_div(M_total, 2 * kRowsPerCta * nc)) + gn) * p.num_n_tiles;
+    const int clusters = static_cast<int>(
+        std::min<long long>(max_tiles, two ? st->clusters_grouped_2c : st->clusters_grouped));
+    const cudaError_t e = two ? launch_grouped_2c(P, 2 * clusters, smem, stream)
+                              : launch_grouped_2cta(P, 2 * clusters, smem, stream);
     if (e != cudaSuccess) return launch_status(e);
   }
   return BWG_OK;

@@ -103,7 +103,7 @@ struct Sched {
     tl.swap_rows = 0;
     if constexpr (GROUPED) {
       grouped_tile(t, p.G, prefix, lo, hi, kTileM, kTileN, &tl.g, &tl.m0, &tl.n0, &tl.row_end);
-      if constexpr (CG == 2) {
+      if constexpr (CG == 2 && NC == 1) {
         if (p.swap_ends) tl.swap_rows = grouped_swap_rows(tl.m0, tl.row_end, kTileM);
         // A swapped tile spans all 256 columns in one unit (its MMA M is the
         // column count): if the last-wave split halved it, the first half
@@ -205,7 +205,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
   if constexpr (GROUPED) {
     if (threadIdx.x == 64) {
       const bool ok = grouped_tables(p.group_offsets, p.g_begin, p.G, p.G_total, p.M,
-                                     p.num_n_tiles, kRowsPerCta * CG, t_prefix, t_lo, t_hi);
+                                     p.num_n_tiles, kRowsPerCta * CG * NC, t_prefix, t_lo, t_hi);
       if (!ok && crank == 0) record_fault(p.err, kFaultBadOffsets, 0, 0, 0, 0);
     }
   }
@@ -572,6 +572,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   gemm_body<2, 1, true, 1>(p, p.base);
 }
 
+// Grouped, two consumers: 512-row units; the second consumer's 256 rows are
+// skipped where a group has 256 rows or fewer left.
+__global__ void __launch_bounds__(kThreads2C, 1)
+    gemm_grouped_2c_kernel(const __grid_constant__ GroupedParams p) {
+  gemm_body<2, 1, true, 2>(p, p.base);
+}
+
 template <class K, class P>
 cudaError_t launch_cluster(K kernel, const P& p, int cg, int grid, size_t smem, cudaStream_t s,
                            int threads = kThreads) {
@@ -608,6 +615,10 @@ cudaError_t launch_gemm_2cta_2c(const GemmParams& p, int grid, size_t smem, cuda
   return launch_cluster(gemm_dense_2c_kernel, p, 2, grid, smem, s, kThreads2C);
 }
 
+cudaError_t launch_grouped_2c(const GroupedParams& p, int grid, size_t smem, cudaStream_t s) {
+  return launch_cluster(gemm_grouped_2c_kernel, p, 2, grid, smem, s, kThreads2C);
+}
+
 cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, cudaStream_t s) {
   return launch_cluster(gemm_grouped_kernel, p, 2, grid, smem, s);
 }
@@ -636,6 +647,11 @@ int max_active_clusters_gemm_2c(size_t smem) {
   return occupancy_clusters(reinterpret_cast<const void*>(gemm_dense_2c_kernel), 2, smem, kThreads2C);
 }
 
+int max_active_clusters_grouped_2c(size_t smem) {
+  return occupancy_clusters(reinterpret_cast<const void*>(gemm_grouped_2c_kernel), 2, smem,
+                            kThreads2C);
+}
+
 int max_active_clusters_gemm(int cluster, bool grouped, size_t smem) {
   const void* fn = grouped ? reinterpret_cast<const void*>(gemm_grouped_kernel)
                    : cluster == 4 ? reinterpret_cast<const void*>(gemm_dense_kernel<2, 2>)
@@ -645,11 +661,12 @@ int max_active_clusters_gemm(int cluster, bool grouped, size_t smem) {
 }
 
 cudaError_t set_gemm_attributes(size_t smem) {
-  const void* fns[5] = {reinterpret_cast<const void*>(gemm_dense_kernel<1, 1>),
+  const void* fns[6] = {reinterpret_cast<const void*>(gemm_dense_kernel<1, 1>),
                         reinterpret_cast<const void*>(gemm_dense_kernel<2, 1>),
                         reinterpret_cast<const void*>(gemm_dense_kernel<2, 2>),
                         reinterpret_cast<const void*>(gemm_dense_2c_kernel),
-                        reinterpret_cast<const void*>(gemm_grouped_kernel)};
+                        reinterpret_cast<const void*>(gemm_grouped_kernel),
+                        reinterpret_cast<const void*>(gemm_grouped_2c_kernel)};
   for (const void* fn : fns) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

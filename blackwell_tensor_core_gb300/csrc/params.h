@@ -83,6 +83,8 @@ cudaError_t launch_gemm_2cta(const GemmParams& p, int grid, size_t smem, cudaStr
 cudaError_t launch_gemm_2cta_mc(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_gemm_2cta_2c(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
 int max_active_clusters_gemm_2c(size_t smem);
+cudaError_t launch_grouped_2c(const GroupedParams& p, int grid, size_t smem, cudaStream_t s);
+int max_active_clusters_grouped_2c(size_t smem);
 cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_small_m(const SmallMParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_zero_fill(void* d, int rows, int cols, int ld, int elt_bytes, cudaStream_t s);

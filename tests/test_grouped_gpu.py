@@ -116,6 +116,7 @@ def test_grouped_swapped_group_ends_exact(counts, monkeypatch):
     Dref, _ = oracle.grouped_gemm(wl.bits(A), [wl.bits(b) for b in Bs], off)
     want = oracle.round_to(Dref, "bf16")
     monkeypatch.setenv("BWG_GROUPED_SWAP", "1")
+    monkeypatch.setenv("BWG_GROUPED_1C", "1")  # swapped ends belong to the one-consumer kernel
     D, st, word = run_grouped(A, Bs, off)
     assert st == 0, hex(word)
     assert_bits_equal(D, want, "swapped ends")
@@ -123,3 +124,20 @@ def test_grouped_swapped_group_ends_exact(counts, monkeypatch):
     D2, st, word = run_grouped(A, Bs, off)
     assert st == 0, hex(word)
     assert_bits_equal(D2, want, "padded ends")
+
+
+@pytest.mark.parametrize("one_consumer", ["0", "1"])
+def test_grouped_both_kernels_exact(one_consumer, monkeypatch):
+    """Groups ending 1..511 rows into a 512-row unit (second consumer skipped
+    at 256 rows or fewer) and the 256-row kernel: both exact."""
+    monkeypatch.setenv("BWG_GROUPED_1C", one_consumer)
+    counts = [1, 255, 256, 257, 511, 512, 513, 0, 700, 1030]
+    off = wl.offsets_from_counts(counts)
+    g = wl.generator(6300)
+    K, N = 128, 520
+    A = wl.randint_matrix(int(off[-1]), K, -2, 2, g)
+    Bs = [wl.randint_matrix(K, N, -2, 2, g) for _ in counts]
+    Dref, _ = oracle.grouped_gemm(wl.bits(A), [wl.bits(b) for b in Bs], off)
+    D, st, word = run_grouped(A, Bs, off)
+    assert st == 0, hex(word)
+    assert_bits_equal(D, oracle.round_to(Dref, "bf16"), "grouped consumers=%s" % one_consumer)
