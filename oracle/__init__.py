@@ -14,6 +14,17 @@ Acceptance (the method's stated bound, one element at a time):
     |D - D_ref| <= 2^-7 * |D_ref| + 1e-3 * S,   S = sum_k |A[i,k]*B[k,j]|
 and bit-exact agreement where inputs are integer-valued and every partial sum
 is exactly representable in binary32.
+
+SwiGLU (``swiglu``, ``grouped_swiglu``, ``swiglu_elements``): H = silu(gate) *
+up on the FP64 GEMM of a [gate | up] weight, computed in ``oracle_swiglu``.
+Its acceptance bound is the GEMM's carried through the activation:
+    |H - H_ref| <= 2^-7 |H_ref| + 1e-3 * W,
+    W = 1.1 |up| S_gate + |silu(gate)| S_up + 1.1e-3 S_gate S_up,
+because an accumulator error e_g <= 1e-3 S_gate moves silu(gate) by at most
+1.1 e_g (|silu'| < 1.1 everywhere), an error e_u <= 1e-3 S_up moves the
+product by |silu(gate)| e_u, the cross term is their product, and the final
+rounding to BF16/FP16 with the activation's own evaluation error stays inside
+2^-7 |H_ref|.
 """
 from __future__ import annotations
 
@@ -67,6 +78,8 @@ def _load():
                                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 dp, dp]
             lib.oracle_grouped_gemm.restype = None
+            lib.oracle_swiglu.argtypes = [dp, ctypes.c_long, ctypes.c_int, dp, dp]
+            lib.oracle_swiglu.restype = None
             lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
             lib.oracle_bf16_to_double.restype = ctypes.c_double
             lib.oracle_fp16_to_double.argtypes = [ctypes.c_uint16]
@@ -195,3 +208,46 @@ def bound_violations(D: np.ndarray, D_ref: np.ndarray, S: np.ndarray,
     err = np.abs(D - D_ref)
     lim = rel * np.abs(D_ref) + abs_frac * S
     return ~(err <= lim)  # NaN counts as a violation
+
+
+def swiglu(D: np.ndarray, with_silu: bool = False):
+    """H = silu(gate) * up for D = [gate | up] ([rows, 2I] float64) -> [rows, I].
+
+    With ``with_silu`` also returns silu(gate) (for the error bound)."""
+    D = np.ascontiguousarray(D, dtype=np.float64)
+    rows, n2 = D.shape
+    if n2 % 2:
+        raise ValueError("D must have an even number of columns: [gate | up]")
+    I = n2 // 2
+    H = np.empty((rows, I), dtype=np.float64)
+    silu = np.empty((rows, I), dtype=np.float64)
+    _load().oracle_swiglu(_ptr(D, ctypes.c_double), rows, I, _ptr(H, ctypes.c_double),
+                          _ptr(silu, ctypes.c_double))
+    return (H, silu) if with_silu else H
+
+
+def swiglu_weight(D: np.ndarray, S: np.ndarray, silu: np.ndarray) -> np.ndarray:
+    """W of the SwiGLU bound (module docstring) from D = [gate | up], S and silu(gate)."""
+    I = D.shape[1] // 2
+    up, s_gate, s_up = D[:, I:], S[:, :I], S[:, I:]
+    return 1.1 * np.abs(up) * s_gate + np.abs(silu) * s_up + 1.1e-3 * s_gate * s_up
+
+
+def grouped_swiglu(A: np.ndarray, Bs: list, offsets: np.ndarray, dtype: str = "bf16"):
+    """Grouped FC1 with SwiGLU: H [rows, N/2] and its bound weight W."""
+    D, S = grouped_gemm(A, Bs, offsets, dtype)
+    H, silu = swiglu(D, with_silu=True)
+    return H, swiglu_weight(D, S, silu)
+
+
+def swiglu_elements(A: np.ndarray, B: np.ndarray, I: np.ndarray, J: np.ndarray, dtype: str = "bf16"):
+    """H[I[t], J[t]] and W for B = [gate | up] ([K, 2*width]), one pair of dot products each."""
+    width = B.shape[1] // 2
+    J = np.asarray(J, dtype=np.int64)
+    I = np.asarray(I, dtype=np.int64)
+    Dg, Sg = gemm_elements(A, B, I, J, dtype)
+    Du, Su = gemm_elements(A, B, I, J + width, dtype)
+    D = np.stack([Dg, Du], axis=1)
+    S = np.stack([Sg, Su], axis=1)
+    H, silu = swiglu(D, with_silu=True)
+    return H[:, 0], swiglu_weight(D, S, silu)[:, 0]

@@ -130,6 +130,38 @@ void oracle_grouped_gemm(const uint16_t *A, const uint16_t *const *Bs, const int
 }
 
 /*
+ * SwiGLU of a gate/up projection computed as one GEMM.
+ *   "B200 的 2CTA 怎样调优", section 七, "Gate／SwiGLU": the output at each
+ *   position is up x SiLU(gate), where the gate and up projections are column
+ *   blocks of the same GEMM; no reduction over a row is involved.
+ *   "MegaMoE … 融合算子解读", section 09: FC1's accumulators become
+ *   gate/up pairs, then SwiGLU, then the next layer's input.
+ * Layout (the library's reading of "column blocks"): D is [rows][2*I], the
+ * gate projection in columns 0 .. I-1 and the up projection in columns
+ * I .. 2I-1 (the weight matrix is [gate | up] along N).  H is [rows][I]:
+ *   H[r][j] = silu(g) * u,   g = D[r][j],  u = D[r][I + j],
+ *   silu(x) = x * sigmoid(x) = x / (1 + exp(-x)).
+ * For x far below zero exp(-x) overflows to +inf and silu(x) is -0, the
+ * limit of x / (1 + e^-x); the true value there is below 1e-300 in size.
+ * SILU, if not NULL, receives silu(g) ([rows][I]) for the error bound.
+ */
+void oracle_swiglu(const double *D, long rows, int I, double *H, double *SILU) {
+    long r;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < rows; ++r) {
+        const double *gate = D + r * 2L * I;
+        const double *up = gate + I;
+        double *h = H + r * (long)I;
+        for (int j = 0; j < I; ++j) {
+            double g = gate[j];
+            double silu = g / (1.0 + exp(-g));
+            h[j] = silu * up[j];
+            if (SILU) SILU[r * (long)I + j] = silu;
+        }
+    }
+}
+
+/*
  * Round-to-nearest-even from double to the 16-bit output formats, written
  * from the format definitions.  Used only where the exact result is known to
  * be representable in binary32 (integer-valued inputs), so the double ->
