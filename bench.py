@@ -349,6 +349,46 @@ def _variant_grouped(ops, wl, stream, dist_mod, peaks, steps, warm, dev):
         "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": tf / peaks["bf16_tflops"]},
         "l2": "A + B (1.34 GB) larger than L2"}
+    del D
+    # the same FC1 with the SwiGLU epilogue: B_g = [gate | up], H = [rows, N/2]
+    H = torch.empty((c.total, c.N // 2), dtype=torch.bfloat16, device=dev)
+    hp = H.data_ptr()
+
+    def slaunch():
+        ops.grouped_gemm_swiglu_bf16(a, bptrs, hp, o, c.G, c.total, c.N, c.K, h)
+    for _ in range(warm):
+        slaunch()
+    _, per = time_launches(slaunch, max(5, steps // 4), stream, dist_mod)
+    check_device_error(ops)
+    ms = statistics.mean(per)
+    tf = c.flops / (ms * 1e-3) / 1e12
+    out["grouped_fc1_swiglu_32x4096x4096"] = {
+        "ms_per_launch": ms, "tflops": tf, "rows": c.total, "out_cols": c.N // 2,
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tf / peaks["bf16_tflops"]},
+        "l2": "A + B (1.34 GB) larger than L2"}
+    del H, A, Bs
+    # expert FC2 (down projection) over the same buckets: K = 2048, N = 4096
+    c2 = wl.grouped_fc2_case()
+    A2 = c2.A.to(dev)
+    B2 = [b.to(dev) for b in c2.Bs]
+    D2 = torch.empty((c2.total, c2.N), dtype=torch.bfloat16, device=dev)
+    b2ptrs = [b.data_ptr() for b in B2]
+    a2, d2 = A2.data_ptr(), D2.data_ptr()
+
+    def flaunch():
+        ops.grouped_gemm_bf16(a2, b2ptrs, d2, o, c2.G, c2.total, c2.N, c2.K, h)
+    for _ in range(warm):
+        flaunch()
+    _, per = time_launches(flaunch, max(5, steps // 4), stream, dist_mod)
+    check_device_error(ops)
+    ms = statistics.mean(per)
+    tf = c2.flops / (ms * 1e-3) / 1e12
+    out["grouped_fc2_32x4096x2048"] = {
+        "ms_per_launch": ms, "tflops": tf, "rows": c2.total,
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tf / peaks["bf16_tflops"]},
+        "l2": "A + B (0.67 GB) larger than L2"}
     return out
 
 

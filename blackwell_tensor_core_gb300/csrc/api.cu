@@ -183,6 +183,19 @@ int group_m_from_env() {
   return g > 0 ? g : kGroupM;
 }
 
+// Scheduling of the two-consumer kernels: units claimed at run time with
+// cluster launch control, or the persistent round-robin loop.  Measured on
+// GB300: the grouped FC1 runs 5% faster dynamic (expert units differ in
+// cost), dense squares the same either way, so the default is dynamic for
+// grouped and static for dense.  BWG_SCHED=clc / static overrides both.
+bool dynamic_sched_from_env(bool by_default) {
+  const char* v = std::getenv("BWG_SCHED");
+  if (v == nullptr) return by_default;
+  if (std::strcmp(v, "clc") == 0) return true;
+  if (std::strcmp(v, "static") == 0) return false;
+  return by_default;
+}
+
 int no_tail_split_from_env() {
   const char* v = std::getenv("BWG_NO_TAIL_SPLIT");
   return (v != nullptr && v[0] == '1') ? 1 : 0;
@@ -273,15 +286,19 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     o->smem_input_per_cta = stages * dense_stage_bytes(cg, nc);
     o->smem_total = dense_smem(cg, stages, direct, nc);
     if (nc == 2) {
-      o->grid = 2 * std::min(o->tiles, max_clusters_2c > 0 ? max_clusters_2c : sm_count / 2);
+      o->workers = std::min(o->tiles, max_clusters_2c > 0 ? max_clusters_2c : sm_count / 2);
+      o->grid = 2 * o->workers;
     } else if (mc == 2) {
       // schedule units are stacks of two pair tiles; 4-CTA clusters
       const int units = ceil_div(ceil_div(M, o->tile_m), 2) * ceil_div(N, o->tile_n);
-      o->grid = 4 * std::min(units, max_clusters_mc > 0 ? max_clusters_mc : sm_count / 4);
+      o->workers = std::min(units, max_clusters_mc > 0 ? max_clusters_mc : sm_count / 4);
+      o->grid = 4 * o->workers;
     } else if (cg == 2) {
-      o->grid = 2 * std::min(o->tiles, max_clusters_2cta > 0 ? max_clusters_2cta : sm_count / 2);
+      o->workers = std::min(o->tiles, max_clusters_2cta > 0 ? max_clusters_2cta : sm_count / 2);
+      o->grid = 2 * o->workers;
     } else {
-      o->grid = std::min(o->tiles, max_ctas_1cta > 0 ? max_ctas_1cta : sm_count);
+      o->workers = std::min(o->tiles, max_ctas_1cta > 0 ? max_ctas_1cta : sm_count);
+      o->grid = o->workers;
     }
     o->tx_bytes = static_cast<uint32_t>(cg * dense_stage_bytes(cg, nc));
     o->idesc = make_idesc_f16(fmt, /*a_mn_major=*/false, /*b_mn_major=*/true, o->mma_m, kTileN);
@@ -291,15 +308,19 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
   if (kind != BWG_KERNEL_SMALL_M) {
     const int per_unit = kind == BWG_KERNEL_2CTA_MC ? 2 : 1;
     const int base_units = ceil_div(ceil_div(M, o->tile_m), per_unit) * ceil_div(N, o->tile_n);
-    const int workers = (kind == BWG_KERNEL_2CTA || kind == BWG_KERNEL_2CTA_2C) ? o->grid / 2
-                        : kind == BWG_KERNEL_2CTA_MC ? o->grid / 4 : o->grid;
     int f = 1;
     const bool two = kind == BWG_KERNEL_2CTA_2C;
     const int R = no_tail_split_from_env()
                       ? 0
-                      : tail_split(base_units, workers, two ? 4 : 2, two ? kCostHalf2 : kCostHalf1,
+                      : tail_split(base_units, o->workers, two ? 4 : 2, two ? kCostHalf2 : kCostHalf1,
                                    kCostQuarter2, &f);
     o->units = base_units - R + R * f;
+    if (two && dynamic_sched_from_env(false)) {
+      o->dynamic = 1;
+      o->grid = 2 * o->units;  // one pair per unit; running pairs claim the rest
+    }
+  } else {
+    o->workers = o->grid;
   }
   return BWG_OK;
 }
@@ -548,18 +569,25 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
     return launch_status(launch_gemm_2cta(p, pl.grid, pl.smem_total, stream));
   if (pl.kernel == BWG_KERNEL_2CTA_MC)
     return launch_status(launch_gemm_2cta_mc(p, pl.grid, pl.smem_total, stream));
+  p.workers = pl.workers;
   if (pl.kernel == BWG_KERNEL_2CTA_2C)
-    return launch_status(launch_gemm_2cta_2c(p, pl.grid, pl.smem_total, stream));
+    return launch_status(launch_gemm_2cta_2c(p, pl.grid, pl.smem_total, stream, pl.dynamic != 0));
   return launch_status(launch_gemm_1cta(p, pl.grid, pl.smem_total, stream));
 }
 
+// swiglu: B_g is [gate | up] with N columns (N/2 each) and D is H [M_total,
+// N/2] = silu(gate) * up.  The up block starts at column N/2, which a TMA
+// load's first coordinate must reach on a 16-byte boundary: N/2 a multiple
+// of 8, i.e. N a multiple of 16.
 bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
                        const int* group_offsets, int G, int M_total, int N, int K,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, bool swiglu = false) {
   if (G < 0 || M_total < 0 || N < 0 || K < 0) return BWG_ERR_INVALID_ARG;
   if (G == 0 || M_total == 0 || N == 0) return BWG_OK;
   if (D == nullptr || group_offsets == nullptr) return BWG_ERR_INVALID_ARG;
   if (!aligned16(D) || (static_cast<long long>(N) * 2) % 16 != 0) return BWG_ERR_ALIGNMENT;
+  if (swiglu && N % 16 != 0) return BWG_ERR_ALIGNMENT;
+  const int n_out = swiglu ? N / 2 : N;  // columns of D
   if (K > 0) {
     if (A == nullptr || B == nullptr) return BWG_ERR_INVALID_ARG;
     if (!aligned16(A) || (static_cast<long long>(K) * 2) % 16 != 0) return BWG_ERR_ALIGNMENT;
@@ -571,7 +599,8 @@ bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
   DeviceState* st = nullptr;
   bwg_status s = ensure_device(&st);
   if (s != BWG_OK) return s;
-  if (K == 0) return launch_status(launch_zero_fill(D, M_total, N, N, 2, stream));
+  // K = 0: every accumulator is 0, and so is silu(0) * 0
+  if (K == 0) return launch_status(launch_zero_fill(D, M_total, n_out, n_out, 2, stream));
   const CUtensorMapDataType in_t =
       fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   // Two MMA consumers (512-row units) unless BWG_GROUPED_1C=1 asks for the
@@ -590,7 +619,7 @@ bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
     if (!get_map(&p.map_a, A, in_t, K, M_total, static_cast<uint64_t>(K) * 2, kBK, kRowsPerCta,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
         !get_map(&p.map_d, D, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                 N, M_total, static_cast<uint64_t>(N) * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+                 n_out, M_total, static_cast<uint64_t>(n_out) * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
       return BWG_ERR_CUDA;
     for (int i = 0; i < gn; ++i)
       if (!get_map(&P.map_b[i], B[g0 + i], in_t, N, K, static_cast<uint64_t>(N) * 2, 64, kBK,
@@ -601,10 +630,11 @@ bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
     p.group_offsets = group_offsets;
     p.timeout_ns = g_timeout_ns.load();
     p.M = M_total;
-    p.N = N;
+    p.N = n_out;
     p.K = K;
-    p.ldd = N;
-    p.num_n_tiles = ceil_div(N, kTileN);
+    p.ldd = n_out;
+    p.num_n_tiles = ceil_div(n_out, swiglu ? kTileN / 2 : kTileN);
+    p.swiglu_up = swiglu ? n_out : 0;
     p.num_m_tiles = 0;
     p.num_k_blocks = ceil_div(K, kBK);
     p.group_m = kGroupM;
@@ -622,15 +652,24 @@ bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
       // tiles here are bound by how fast shared memory fills, so it measured
       // no faster than the padded tile.  BWG_GROUPED_SWAP=1 turns it on.
       const char* v = std::getenv("BWG_GROUPED_SWAP");
-      p.swap_ends = (v != nullptr && v[0] == '1') ? 1 : 0;
+      p.swap_ends = (v != nullptr && v[0] == '1' && !swiglu) ? 1 : 0;
     }
     // Upper bound on tiles: every group adds at most one partial row tile.
     const long long max_tiles =
         (static_cast<long long>(ceil_div(M_total, 2 * kRowsPerCta * nc)) + gn) * p.num_n_tiles;
     const int clusters = static_cast<int>(
         std::min<long long>(max_tiles, two ? st->clusters_grouped_2c : st->clusters_grouped));
-    const cudaError_t e = two ? launch_grouped_2c(P, 2 * clusters, smem, stream)
-                              : launch_grouped_2cta(P, 2 * clusters, smem, stream);
+    // Dynamic scheduling: one pair per unit.  The tile count is known only on
+    // the device; the units of a last wave cut in up to 4 parts are at most
+    // tiles + 3 x (pairs running at once), and pairs past the end claim or
+    // find nothing.
+    const bool dyn = two && dynamic_sched_from_env(true);
+    p.workers = clusters;
+    const long long grid_pairs = dyn ? max_tiles + 3LL * clusters : clusters;
+    if (2 * grid_pairs > 0x7fffffffLL) return BWG_ERR_UNSUPPORTED;
+    const cudaError_t e =
+        two ? launch_grouped_2c(P, static_cast<int>(2 * grid_pairs), smem, stream, swiglu, dyn)
+            : launch_grouped_2cta(P, 2 * clusters, smem, stream, swiglu);
     if (e != cudaSuccess) return launch_status(e);
   }
   return BWG_OK;
@@ -781,6 +820,20 @@ bwg_status grouped_gemm_fp16(const void* A, const void* const* B, void* D, const
                              int G, int M_total, int N, int K, void* stream) {
   return run_grouped(true, A, B, D, group_offsets, G, M_total, N, K,
                      static_cast<cudaStream_t>(stream));
+}
+
+bwg_status grouped_gemm_swiglu_bf16(const void* A, const void* const* B, void* H,
+                                    const int* group_offsets, int G, int M_total, int N, int K,
+                                    void* stream) {
+  return run_grouped(false, A, B, H, group_offsets, G, M_total, N, K,
+                     static_cast<cudaStream_t>(stream), true);
+}
+
+bwg_status grouped_gemm_swiglu_fp16(const void* A, const void* const* B, void* H,
+                                    const int* group_offsets, int G, int M_total, int N, int K,
+                                    void* stream) {
+  return run_grouped(true, A, B, H, group_offsets, G, M_total, N, K,
+                     static_cast<cudaStream_t>(stream), true);
 }
 
 bwg_status gemm_bf16_small_m_noalloc(const void* A, const void* B, void* D, int M, int N, int K,

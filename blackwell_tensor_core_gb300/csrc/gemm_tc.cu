@@ -37,7 +37,20 @@ constexpr uint32_t kAStageBytes = kRowsPerCta * kBK * 2;  // 16 KiB: 128 rows x 
 constexpr uint32_t kBChunkBytes = 64 * kBK * 2;           // 8 KiB: 64 K rows x 64 N
 
 enum : uint32_t { kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2 };
-enum : uint32_t { kBarFull = 0, kBarEmpty = 1, kBarAccFull = 2, kBarAccEmpty = 3 };
+enum : uint32_t {
+  kBarFull = 0,
+  kBarEmpty = 1,
+  kBarAccFull = 2,
+  kBarAccEmpty = 3,
+  kBarClcFull = 4,   // a cluster-launch-control response has landed
+  kBarClcEmpty = 5   // every role of both CTAs has read a response slot
+};
+
+// Dynamic (cluster launch control) scheduling: response slots per CTA.  The
+// leader's producer asks for the next unit when it starts a unit, so a pair
+// holds at most one unit in reserve; the slots only give the slower roles
+// (MMA, epilogue) room to read responses later.
+constexpr uint32_t kClcSlots = 4;
 
 __device__ __forceinline__ void record_fault(unsigned long long* err, unsigned long long kind,
                                              uint32_t role, uint32_t bar, uint32_t stage,
@@ -65,9 +78,12 @@ struct Tile {
 // MC pairs per cluster (1, or 2 when the pairs share B through TMA multicast):
 // a schedule unit is then a stack of MC tiles along M with the same columns,
 // and pair `pair` of the cluster takes tile row (unit row * MC + pair).
-template <int CG, int MC, bool GROUPED, int NC = 1>
+// SW (fused SwiGLU): a tile's 256 MMA columns are 128 gate and 128 up
+// columns, so it covers 128 output columns; n0 counts output columns.
+template <int CG, int MC, bool GROUPED, int NC = 1, bool SW = false>
 struct Sched {
   static constexpr int kTileM = kRowsPerCta * CG * NC;
+  static constexpr int kOutCols = SW ? kTileN / 2 : kTileN;  // output columns of a whole tile
   const GemmParams& p;
   const int* prefix;  // grouped tables in shared memory: prefix[G+1], lo[G], hi[G]
   const int* lo;
@@ -98,12 +114,12 @@ struct Sched {
     Tile tl;
     int t, part, parts;
     unit_part(u, tiles, split, f, &t, &part, &parts);
-    int col_off = parts == 1 ? 0 : (part & 1) * (kTileN / 2);
+    int col_off = parts == 1 ? 0 : (part & 1) * (kOutCols / 2);
     tl.width = parts == 1 ? kTileN : kTileN / 2;
     tl.swap_rows = 0;
     if constexpr (GROUPED) {
-      grouped_tile(t, p.G, prefix, lo, hi, kTileM, kTileN, &tl.g, &tl.m0, &tl.n0, &tl.row_end);
-      if constexpr (CG == 2 && NC == 1) {
+      grouped_tile(t, p.G, prefix, lo, hi, kTileM, kOutCols, &tl.g, &tl.m0, &tl.n0, &tl.row_end);
+      if constexpr (CG == 2 && NC == 1 && !SW) {
         if (p.swap_ends) tl.swap_rows = grouped_swap_rows(tl.m0, tl.row_end, kTileM);
         // A swapped tile spans all 256 columns in one unit (its MMA M is the
         // column count): if the last-wave split halved it, the first half
@@ -154,10 +170,36 @@ __device__ __forceinline__ const CUtensorMap* b_map(const PT& P, int g) {
     return &P.map_b;
 }
 
+// SwiGLU of one gate/up accumulator pair: silu(g) * u with
+// silu(g) = g * sigmoid(g) = g / (1 + e^-g), using the hardware's
+// approximate exponential and reciprocal (a few ulp of FP32, far below the
+// final rounding to 16 bits).  For very negative g, e^-g overflows to +inf,
+// the reciprocal is 0 and the result a signed zero, the function's limit.
+__device__ __forceinline__ float swiglu_f32(float g, float u) {
+  return g * rcp_approx(1.0f + __expf(-g)) * u;
+}
+
 // NC = MMA consumers per pair (1, or 2 for 512x256 tiles: two A blocks per
 // stage share one B stage, each consumer owning half of the TMEM columns).
-template <int CG, int MC, bool GROUPED, int NC, class PT>
+// SW = fused SwiGLU epilogue ("B200 的 2CTA 怎样调优", section 七,
+// Gate/SwiGLU: pair the gate and up column blocks of one GEMM in the
+// epilogue).  B is [gate | up] along N; CTA 0 of the pair loads gate columns
+// and CTA 1 the matching up columns, so in every CTA's accumulator the first
+// half of the MMA columns is gate and the second half up, for the same rows,
+// and each epilogue thread finds both values of a pair in its own TMEM lane.
+//
+// DYN = dynamic scheduling by cluster launch control ("从 CUDA 代码到 GPU
+// 执行" section 9; "B200 的 2CTA 怎样调优": with CTA pairs the claim is per
+// cluster, so both CTAs get the same unit).  The grid has one cluster per
+// unit; a cluster starts with the unit of its own index and, while it works,
+// its leader's producer asks the hardware to cancel a cluster that has not
+// launched yet and takes over that cluster's unit.  The response is
+// multicast into both CTAs; every role reads the responses in order, so the
+// producer, MMA and epilogue warps of both CTAs walk the same unit sequence.
+template <int CG, int MC, bool GROUPED, int NC, bool SW, bool DYN, class PT>
 __device__ void gemm_body(const PT& P, const GemmParams& p) {
+  static_assert(!SW || (CG == 2 && MC == 1 && GROUPED), "SwiGLU runs on the grouped pair kernels");
+  static_assert(!DYN || (CG == 2 && MC == 1 && NC == 2), "dynamic scheduling: two-consumer pairs");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t warp = threadIdx.x >> 5;
@@ -183,6 +225,15 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
   auto acc_empty_bar = [&](int a) { return smem_bar + 8u * (2 * S + 2 + a); };
   const uint32_t tmem_slot = smem_bar + 8u * (2 * S + 4);
   const uint32_t tables = tmem_slot + 16u;
+  // CLC responses (16 bytes each, 16-byte aligned) and their barriers, after
+  // the grouped tables
+  const uint32_t clc = (tables + 4u * (3u * kMaxGroupsPerLaunch + 1u) + 15u) & ~15u;
+  auto clc_resp = [&](uint32_t s) { return clc + 16u * s; };
+  auto clc_full = [&](uint32_t s) { return clc + 16u * kClcSlots + 8u * s; };
+  auto clc_empty = [&](uint32_t s) { return clc + 16u * kClcSlots + 8u * (kClcSlots + s); };
+  // readers of each response: the producer of each CTA, the leader's MMA
+  // threads, and every epilogue warp of both CTAs
+  constexpr uint32_t kClcReaders = 2u + NC + 8u * NC;
 
   // ---- set-up: barriers, grouped tables, TMEM allocation -----------------
   if (threadIdx.x == 0) {
@@ -194,6 +245,12 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
     for (int a = 0; a < 2; ++a) {
       mbar_init(acc_full_bar(a), 1);
       mbar_init(acc_empty_bar(a), CG * 4);
+    }
+    if constexpr (DYN) {
+      for (uint32_t s = 0; s < kClcSlots; ++s) {
+        mbar_init(clc_full(s), 1);
+        mbar_init(clc_empty(s), kClcReaders);
+      }
     }
     fence_mbarrier_init();
   }
@@ -228,16 +285,66 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
 
   const int first = static_cast<int>((CG == 2) ? cluster_id_x() : blockIdx.x);
   const int stride = static_cast<int>((CG == 2) ? num_clusters_x() : gridDim.x);
-  const Sched<CG, MC, GROUPED, NC> sched(p, t_prefix, t_lo, t_hi, stride, static_cast<int>(pair));
+  // the last-wave cut counts the pairs that run at once: the grid with the
+  // static schedule, the co-resident pairs with the dynamic one
+  const Sched<CG, MC, GROUPED, NC, SW> sched(p, t_prefix, t_lo, t_hi, DYN ? p.workers : stride,
+                                             static_cast<int>(pair));
   const int total = sched.total();
   bool aborted = false;
+
+  // Next unit of this CTA's sequence after unit t: t + stride (static), or the
+  // unit of response k (dynamic; -1 when no launch was cancelled, which ends
+  // the sequence, or when the wait timed out).  `arm` re-arms the slot for its
+  // next response (the producer of each CTA does this); `warp_wide`: all 32
+  // lanes read the response and lane 0 releases the slot for the warp.
+  auto next_unit = [&](int t, uint32_t& k, uint32_t role, bool arm, bool warp_wide) -> int {
+    if constexpr (!DYN) {
+      return t + stride;
+    } else {
+      const uint32_t s = k % kClcSlots;
+      const uint32_t ph = (k / kClcSlots) & 1u;
+      const bool got = warp_wide ? warp_wait(clc_full(s), ph, p.timeout_ns)
+                                 : mbar_wait(clc_full(s), ph, p.timeout_ns);
+      if (!got) {
+        if (!warp_wide || lane == 0) record_fault(p.err, kFaultTimeout, role, kBarClcFull, s, ph);
+        aborted = true;
+        return -1;
+      }
+      uint32_t x = 0;
+      const bool ok = clc_query(clc_resp(s), &x);
+      if (ok && arm) mbar_arrive_expect_tx(clc_full(s), 16);
+      if (warp_wide) __syncwarp();
+      if (!warp_wide || lane == 0) mbar_arrive_cluster(mapa_shared(clc_empty(s), leader));
+      ++k;
+      return ok ? static_cast<int>(x) / CG : -1;
+    }
+  };
 
   if (warp == 0) {
     // ---- TMA producer: one thread streams A and B k-blocks into the ring ----
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      for (int t = first; t < total && !aborted; t += stride) {
+      uint32_t k = 0;  // CLC responses read so far
+      if constexpr (DYN) {
+        for (uint32_t c = 0; c < kClcSlots; ++c) mbar_arrive_expect_tx(clc_full(c), 16);
+      }
+      for (int t = first; DYN ? t >= 0 : t < total;
+           t = next_unit(t, k, kRoleProducer, /*arm=*/true, /*warp_wide=*/false)) {
+        if constexpr (DYN) {
+          if (rank == 0) {
+            // ask for the unit after this one (response k), once its slot is free
+            const uint32_t cs = k % kClcSlots;
+            const uint32_t cph = ((k / kClcSlots) & 1u) ^ 1u;
+            if (!mbar_wait(clc_empty(cs), cph, p.timeout_ns)) {
+              record_fault(p.err, kFaultTimeout, kRoleProducer, kBarClcEmpty, cs, cph);
+              aborted = true;
+              break;
+            }
+            clc_try_cancel_multicast(clc_resp(cs), clc_full(cs));
+          }
+        }
+        if (t >= total) continue;  // a unit past the end (grid rounding): nothing to load
         const Tile tl = sched.at(t);
         if (tl.width == 0) continue;
         const uint32_t b_cols = static_cast<uint32_t>(tl.width) / CG;  // this CTA's B columns
@@ -252,7 +359,10 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
             p.tx_extra;
         const int a_row = tl.swap_rows > 0 ? tl.m0 + static_cast<int>(rank * half_rows)
                                            : tl.m0 + static_cast<int>(rank) * kRowsPerCta;
-        const int b_col = tl.n0 + static_cast<int>(rank * b_cols);
+        // SwiGLU: rank 0 loads gate columns n0.., rank 1 the up columns
+        // swiglu_up + n0.. (the same output columns).
+        const int b_col = SW ? tl.n0 + static_cast<int>(rank) * p.swiglu_up
+                             : tl.n0 + static_cast<int>(rank * b_cols);
         const CUtensorMap* mb = b_map<CG, GROUPED>(P, tl.g);
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, p.timeout_ns)) {
@@ -292,6 +402,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
             ph ^= 1u;
           }
         }
+        if (aborted) break;
       }
     }
     __syncwarp();
@@ -310,7 +421,10 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
       uint32_t ph = 0;
       int acc = NC == 1 ? 0 : cons;  // accumulator slot: alternating, or the consumer's own
       uint32_t acc_ph = 0;
-      for (int t = first; t < total && !aborted; t += stride) {
+      uint32_t k = 0;
+      for (int t = first; DYN ? t >= 0 : t < total;
+           t = next_unit(t, k, kRoleMma, /*arm=*/false, /*warp_wide=*/false)) {
+        if (t >= total) continue;
         const Tile tl = sched.at(t);
         if (tl.width == 0) continue;
         if (!((tl.cmask >> cons) & 1)) {
@@ -332,6 +446,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
               ph ^= 1u;
             }
           }
+          if (aborted) break;
           continue;
         }
         if (!mbar_wait(acc_empty_bar(acc), acc_ph ^ 1u, p.timeout_ns)) {
@@ -403,7 +518,10 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
     int acc = NC == 1 ? 0 : cons;
     uint32_t acc_ph = 0;
     uint32_t buf = 0;
-    for (int t = first; t < total; t += stride) {
+    uint32_t k = 0;
+    for (int t = first; DYN ? t >= 0 : t < total;
+         t = next_unit(t, k, kRoleEpilogue, /*arm=*/false, /*warp_wide=*/true)) {
+      if (t >= total) continue;
       const Tile tl = sched.at(t);
       if (tl.width == 0 || !((tl.cmask >> cons) & 1)) continue;
       if (!warp_wait(acc_full_bar(acc), acc_ph, p.timeout_ns)) {
@@ -453,17 +571,49 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         continue;
       }
       const int sub_cols = out32 ? 32 : 64;
-      const int nsub = tl.width / sub_cols;
+      // SwiGLU: the unit's output columns are half its MMA columns (16-bit
+      // output only); gate of output column c is TMEM column c, up is
+      // TMEM column width/2 + c.
+      const int out_cols = SW ? tl.width / 2 : tl.width;
+      const int nsub = out_cols / sub_cols;
+      // Hand the accumulator back to the MMA warp as soon as its last TMEM
+      // read has completed (before the conversion of that last chunk): with
+      // two consumers each owns one accumulator, so its next tile's MMAs wait
+      // for this.
+      auto release_acc = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
+      };
       for (int sub = 0; sub < nsub; ++sub) {
         uint32_t pk[32];
-        if (out32) {
+        const bool last = sub == nsub - 1;
+        if constexpr (SW) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t g[32], u[32];
+            tmem_ld_32x32b_x32(t_acc + sub * 64 + h * 32, g);
+            tmem_ld_32x32b_x32(t_acc + out_cols + sub * 64 + h * 32, u);
+            tmem_wait_ld();
+            if (last && h == 1) release_acc();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float y0 = swiglu_f32(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]));
+              const float y1 =
+                  swiglu_f32(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]));
+              pk[16 * h + i] = outbf ? pack_bf16x2(y0, y1) : pack_f16x2(y0, y1);
+            }
+          }
+        } else if (out32) {
           tmem_ld_32x32b_x32(t_acc + sub * 32, pk);
           tmem_wait_ld();
+          if (last) release_acc();
         } else {
           uint32_t v0[32], v1[32];
           tmem_ld_32x32b_x32(t_acc + sub * 64, v0);
           tmem_ld_32x32b_x32(t_acc + sub * 64 + 32, v1);
           tmem_wait_ld();
+          if (last) release_acc();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float lo0 = __uint_as_float(v0[2 * i]), hi0 = __uint_as_float(v0[2 * i + 1]);
@@ -471,12 +621,6 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
             pk[i] = outbf ? pack_bf16x2(lo0, hi0) : pack_f16x2(lo0, hi0);
             pk[16 + i] = outbf ? pack_bf16x2(lo1, hi1) : pack_f16x2(lo1, hi1);
           }
-        }
-        if (sub == nsub - 1) {
-          // Last TMEM read of this accumulator: hand it back to the MMA warp.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
         }
         const int col0 = tl.n0 + sub * sub_cols;
         if (col0 >= p.N) continue;
@@ -557,26 +701,30 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
 
 template <int CG, int MC>
 __global__ void __launch_bounds__(kThreads, 1) gemm_dense_kernel(const __grid_constant__ GemmParams p) {
-  gemm_body<CG, MC, false, 1>(p, p);
+  gemm_body<CG, MC, false, 1, false, false>(p, p);
 }
 
 // 512x256 tiles on a pair: warp 0 TMA, warps 1-2 MMA (one per consumer),
 // warp 3 idle, warps 4-7 and 8-11 the epilogue of consumer 0 and 1.
+// DYN: one cluster per unit, units claimed by cluster launch control.
+template <bool DYN>
 __global__ void __launch_bounds__(kThreads2C, 1)
     gemm_dense_2c_kernel(const __grid_constant__ GemmParams p) {
-  gemm_body<2, 1, false, 2>(p, p);
+  gemm_body<2, 1, false, 2, false, DYN>(p, p);
 }
 
+template <bool SW>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_grouped_kernel(const __grid_constant__ GroupedParams p) {
-  gemm_body<2, 1, true, 1>(p, p.base);
+  gemm_body<2, 1, true, 1, SW, false>(p, p.base);
 }
 
 // Grouped, two consumers: 512-row units; the second consumer's 256 rows are
 // skipped where a group has 256 rows or fewer left.
+template <bool SW, bool DYN>
 __global__ void __launch_bounds__(kThreads2C, 1)
     gemm_grouped_2c_kernel(const __grid_constant__ GroupedParams p) {
-  gemm_body<2, 1, true, 2>(p, p.base);
+  gemm_body<2, 1, true, 2, SW, DYN>(p, p.base);
 }
 
 template <class K, class P>
@@ -611,16 +759,27 @@ cudaError_t launch_gemm_2cta_mc(const GemmParams& p, int grid, size_t smem, cuda
   return launch_cluster(gemm_dense_kernel<2, 2>, p, 4, grid, smem, s);
 }
 
-cudaError_t launch_gemm_2cta_2c(const GemmParams& p, int grid, size_t smem, cudaStream_t s) {
-  return launch_cluster(gemm_dense_2c_kernel, p, 2, grid, smem, s, kThreads2C);
+cudaError_t launch_gemm_2cta_2c(const GemmParams& p, int grid, size_t smem, cudaStream_t s,
+                                bool dynamic) {
+  return dynamic ? launch_cluster(gemm_dense_2c_kernel<true>, p, 2, grid, smem, s, kThreads2C)
+                 : launch_cluster(gemm_dense_2c_kernel<false>, p, 2, grid, smem, s, kThreads2C);
 }
 
-cudaError_t launch_grouped_2c(const GroupedParams& p, int grid, size_t smem, cudaStream_t s) {
-  return launch_cluster(gemm_grouped_2c_kernel, p, 2, grid, smem, s, kThreads2C);
+cudaError_t launch_grouped_2c(const GroupedParams& p, int grid, size_t smem, cudaStream_t s,
+                              bool swiglu, bool dynamic) {
+  if (dynamic)
+    return swiglu
+               ? launch_cluster(gemm_grouped_2c_kernel<true, true>, p, 2, grid, smem, s, kThreads2C)
+               : launch_cluster(gemm_grouped_2c_kernel<false, true>, p, 2, grid, smem, s, kThreads2C);
+  return swiglu
+             ? launch_cluster(gemm_grouped_2c_kernel<true, false>, p, 2, grid, smem, s, kThreads2C)
+             : launch_cluster(gemm_grouped_2c_kernel<false, false>, p, 2, grid, smem, s, kThreads2C);
 }
 
-cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, cudaStream_t s) {
-  return launch_cluster(gemm_grouped_kernel, p, 2, grid, smem, s);
+cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, cudaStream_t s,
+                                bool swiglu) {
+  return swiglu ? launch_cluster(gemm_grouped_kernel<true>, p, 2, grid, smem, s)
+                : launch_cluster(gemm_grouped_kernel<false>, p, 2, grid, smem, s);
 }
 
 static int occupancy_clusters(const void* fn, int cg, size_t smem, int threads = kThreads) {
@@ -644,16 +803,17 @@ static int occupancy_clusters(const void* fn, int cg, size_t smem, int threads =
 }
 
 int max_active_clusters_gemm_2c(size_t smem) {
-  return occupancy_clusters(reinterpret_cast<const void*>(gemm_dense_2c_kernel), 2, smem, kThreads2C);
-}
-
-int max_active_clusters_grouped_2c(size_t smem) {
-  return occupancy_clusters(reinterpret_cast<const void*>(gemm_grouped_2c_kernel), 2, smem,
+  return occupancy_clusters(reinterpret_cast<const void*>(gemm_dense_2c_kernel<false>), 2, smem,
                             kThreads2C);
 }
 
+int max_active_clusters_grouped_2c(size_t smem) {
+  return occupancy_clusters(reinterpret_cast<const void*>(gemm_grouped_2c_kernel<false, false>), 2,
+                            smem, kThreads2C);
+}
+
 int max_active_clusters_gemm(int cluster, bool grouped, size_t smem) {
-  const void* fn = grouped ? reinterpret_cast<const void*>(gemm_grouped_kernel)
+  const void* fn = grouped ? reinterpret_cast<const void*>(gemm_grouped_kernel<false>)
                    : cluster == 4 ? reinterpret_cast<const void*>(gemm_dense_kernel<2, 2>)
                    : cluster == 2 ? reinterpret_cast<const void*>(gemm_dense_kernel<2, 1>)
                                   : reinterpret_cast<const void*>(gemm_dense_kernel<1, 1>);
@@ -661,12 +821,17 @@ int max_active_clusters_gemm(int cluster, bool grouped, size_t smem) {
 }
 
 cudaError_t set_gemm_attributes(size_t smem) {
-  const void* fns[6] = {reinterpret_cast<const void*>(gemm_dense_kernel<1, 1>),
-                        reinterpret_cast<const void*>(gemm_dense_kernel<2, 1>),
-                        reinterpret_cast<const void*>(gemm_dense_kernel<2, 2>),
-                        reinterpret_cast<const void*>(gemm_dense_2c_kernel),
-                        reinterpret_cast<const void*>(gemm_grouped_kernel),
-                        reinterpret_cast<const void*>(gemm_grouped_2c_kernel)};
+  const void* fns[] = {reinterpret_cast<const void*>(gemm_dense_kernel<1, 1>),
+                       reinterpret_cast<const void*>(gemm_dense_kernel<2, 1>),
+                       reinterpret_cast<const void*>(gemm_dense_kernel<2, 2>),
+                       reinterpret_cast<const void*>(gemm_dense_2c_kernel<false>),
+                       reinterpret_cast<const void*>(gemm_dense_2c_kernel<true>),
+                       reinterpret_cast<const void*>(gemm_grouped_kernel<false>),
+                       reinterpret_cast<const void*>(gemm_grouped_kernel<true>),
+                       reinterpret_cast<const void*>(gemm_grouped_2c_kernel<false, false>),
+                       reinterpret_cast<const void*>(gemm_grouped_2c_kernel<true, false>),
+                       reinterpret_cast<const void*>(gemm_grouped_2c_kernel<false, true>),
+                       reinterpret_cast<const void*>(gemm_grouped_2c_kernel<true, true>)};
   for (const void* fn : fns) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

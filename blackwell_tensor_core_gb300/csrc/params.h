@@ -52,6 +52,8 @@ struct GemmParams {
   int direct_store;          // 1: epilogue stores rows from registers (no staging, one more stage)
   int swap_ends;             // grouped: 1 = compute group ends of <= 128 rows with swapped operands
   uint32_t idesc_swap;       // grouped: descriptor of the swapped MMA (A MN-major, B K-major)
+  int swiglu_up;             // SwiGLU kernels: first column of the up block in B (= N of H)
+  int workers;               // dynamic scheduling: CTA pairs that run at once (last-wave cut)
 };
 
 struct GroupedParams {
@@ -81,11 +83,16 @@ struct SmallMParams {
 cudaError_t launch_gemm_1cta(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_gemm_2cta(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_gemm_2cta_mc(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
-cudaError_t launch_gemm_2cta_2c(const GemmParams& p, int grid, size_t smem, cudaStream_t s);
+// dynamic: cluster-launch-control scheduling (grid = one pair per unit)
+cudaError_t launch_gemm_2cta_2c(const GemmParams& p, int grid, size_t smem, cudaStream_t s,
+                                bool dynamic = false);
 int max_active_clusters_gemm_2c(size_t smem);
-cudaError_t launch_grouped_2c(const GroupedParams& p, int grid, size_t smem, cudaStream_t s);
+// Grouped launchers; swiglu = the fused SwiGLU epilogue over a [gate | up] B.
+cudaError_t launch_grouped_2c(const GroupedParams& p, int grid, size_t smem, cudaStream_t s,
+                              bool swiglu = false, bool dynamic = false);
 int max_active_clusters_grouped_2c(size_t smem);
-cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, cudaStream_t s,
+                                bool swiglu = false);
 cudaError_t launch_small_m(const SmallMParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_zero_fill(void* d, int rows, int cols, int ld, int elt_bytes, cudaStream_t s);
 

@@ -129,6 +129,48 @@ BWG_DEV bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   }
 }
 
+// ---------------------------------------------------------------- math ----
+
+// Hardware approximate reciprocal (flushes subnormal inputs and results to
+// zero; 1/inf = 0).
+BWG_DEV float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------ cluster launch control ---
+// "从 CUDA 代码到 GPU 执行" section 9 (CLC): a running cluster asks to cancel
+// the launch of a cluster that has not started yet; if that succeeds it does
+// that cluster's work itself.  The request is asynchronous: its 16-byte
+// response lands in shared memory at `resp` and completes 16 transaction
+// bytes on the mbarrier `bar`.  With multicast::cluster::all both land at the
+// same offsets in every CTA of the cluster, so one thread asks for the pair.
+BWG_DEV void clc_try_cancel_multicast(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+      ".multicast::cluster::all.b128 [%0], [%1];" ::"r"(resp),
+      "r"(bar)
+      : "memory");
+}
+
+// Decode a response in shared memory: whether a launch was cancelled and, if
+// so, the x index of the first CTA of the cancelled cluster.
+BWG_DEV bool clc_query(uint32_t resp, uint32_t* first_ctaid_x) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .b128 R;\n\t.reg .pred P;\n\t"
+      "ld.shared.b128 R, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 P, R;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t"
+      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, R;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "r"(resp)
+      : "memory");
+  *first_ctaid_x = x;
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------- TMA -----
 
 BWG_DEV void prefetch_tensormap(const CUtensorMap* map) {

@@ -43,7 +43,8 @@ class PlanInfo(ctypes.Structure):
                 ("stages", ctypes.c_int), ("tiles", ctypes.c_int), ("k_blocks", ctypes.c_int),
                 ("coverage", ctypes.c_double), ("smem_input_per_cta", ctypes.c_int),
                 ("smem_total", ctypes.c_int), ("grid", ctypes.c_int), ("tx_bytes", ctypes.c_uint32),
-                ("idesc", ctypes.c_uint32), ("units", ctypes.c_int), ("streamk", ctypes.c_int)]
+                ("idesc", ctypes.c_uint32), ("units", ctypes.c_int), ("streamk", ctypes.c_int),
+                ("workers", ctypes.c_int), ("dynamic", ctypes.c_int)]
 
 
 def lib() -> ctypes.CDLL:
@@ -60,7 +61,8 @@ def lib() -> ctypes.CDLL:
                 f = getattr(L, name)
                 f.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp]
                 f.restype = i
-            for name in ("grouped_gemm_bf16", "grouped_gemm_fp16"):
+            for name in ("grouped_gemm_bf16", "grouped_gemm_fp16", "grouped_gemm_swiglu_bf16",
+                         "grouped_gemm_swiglu_fp16"):
                 f = getattr(L, name)
                 f.argtypes = [vp, ctypes.POINTER(vp), vp, vp, i, i, i, i, vp]
                 f.restype = i
@@ -170,8 +172,11 @@ def gemm_fp16(A_ptr: int, B_ptr: int, D_ptr: int, M: int, N: int, K: int, lda: i
 
 
 def grouped_gemm(A: torch.Tensor, Bs: list, group_offsets: torch.Tensor,
-                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Grouped expert product through grouped_gemm_bf16 / grouped_gemm_fp16."""
+                 out: torch.Tensor | None = None, stream=None, swiglu: bool = False) -> torch.Tensor:
+    """Grouped expert product through grouped_gemm_bf16 / grouped_gemm_fp16.
+
+    With ``swiglu`` each weight is [gate | up] ([K, N]) and the result is
+    silu(gate) * up, [M_total, N/2], through grouped_gemm_swiglu_bf16/_fp16."""
     if A.dtype not in (torch.bfloat16, torch.float16):
         raise TypeError("A must be bfloat16 or float16")
     M_total, K = A.shape
@@ -184,9 +189,15 @@ def grouped_gemm(A: torch.Tensor, Bs: list, group_offsets: torch.Tensor,
         raise ValueError("group_offsets must be a CUDA int32 tensor with G+1 entries")
     if not A.is_contiguous():
         raise ValueError("A must be dense [M_total, K]")
+    n_out = N // 2 if swiglu else N
     if out is None:
-        out = torch.empty((M_total, N), dtype=A.dtype, device=A.device)
-    fn = grouped_gemm_bf16 if A.dtype == torch.bfloat16 else grouped_gemm_fp16
+        out = torch.empty((M_total, n_out), dtype=A.dtype, device=A.device)
+    elif out.shape != (M_total, n_out) or out.dtype != A.dtype or not out.is_contiguous():
+        raise ValueError("out must be a dense [M_total, %d] tensor of A's dtype" % n_out)
+    if swiglu:
+        fn = grouped_gemm_swiglu_bf16 if A.dtype == torch.bfloat16 else grouped_gemm_swiglu_fp16
+    else:
+        fn = grouped_gemm_bf16 if A.dtype == torch.bfloat16 else grouped_gemm_fp16
     fn(A.data_ptr(), [b.data_ptr() for b in Bs], out.data_ptr(), group_offsets.data_ptr(), G, M_total,
        N, K, _stream_handle(stream, A.device))
     return out
@@ -252,3 +263,19 @@ def plan(M: int, N: int, K: int, out_dtype: int = OUT_BF16, sm_count: int = 152,
 def check_gemm_args(A: int, B: int, D: int, M: int, N: int, K: int, lda: int, ldb: int, ldd: int,
                     out_dtype: int) -> int:
     return int(lib().bwg_check_gemm_args(A, B, D, M, N, K, lda, ldb, ldd, out_dtype))
+
+
+def grouped_gemm_swiglu_bf16(A_ptr: int, B_ptrs: list, H_ptr: int, offsets_ptr: int, G: int,
+                             M_total: int, N: int, K: int, stream: int) -> None:
+    p, keep = _ptr_array(B_ptrs)
+    _check(lib().grouped_gemm_swiglu_bf16(A_ptr, p, H_ptr, offsets_ptr, G, M_total, N, K, stream),
+           "grouped_gemm_swiglu_bf16")
+    del keep
+
+
+def grouped_gemm_swiglu_fp16(A_ptr: int, B_ptrs: list, H_ptr: int, offsets_ptr: int, G: int,
+                             M_total: int, N: int, K: int, stream: int) -> None:
+    p, keep = _ptr_array(B_ptrs)
+    _check(lib().grouped_gemm_swiglu_fp16(A_ptr, p, H_ptr, offsets_ptr, G, M_total, N, K, stream),
+           "grouped_gemm_swiglu_fp16")
+    del keep

@@ -16,7 +16,12 @@ Workloads (shapes and value distributions of the method's five cases):
   4  small_m   M=72, N=16384, K=7168, N(0,1)*0.02, BF16 output
   5  grouped   32 experts, 32768 routed rows (top-8 of 4096 tokens), per-expert
                counts from a seeded multinomial, K=N=4096, A ~ N(0,1),
-               B_g ~ N(0, 0.02), BF16 output
+               B_g ~ N(0, 0.02), BF16 output (FC1; with SwiGLU, B_g = [gate | up])
+  6  fc2       the same expert buckets (counts drawn as in 5), K=2048 (the
+               SwiGLU width), N=4096, A ~ N(0,1), B_g ~ N(0, 0.02), BF16 output
+
+Every case takes ``dtype`` ("bf16" or "fp16"): the same draws rounded to the
+other input type (the FP16 runs use FP16 output).
 """
 from __future__ import annotations
 
@@ -113,44 +118,63 @@ class Grouped:
         return 2 * self.total * self.N * self.K
 
 
-def tile_case(seed: int = 1001) -> Dense:
+def _out_for(dtype: str) -> int:
+    return OUT_FP16 if dtype == "fp16" else OUT_BF16
+
+
+def tile_case(seed: int = 1001, dtype: str = "bf16") -> Dense:
     g = generator(seed)
-    A = randint_matrix(256, 512, -2, 2, g)
-    B = randint_matrix(512, 256, -2, 2, g)
-    return Dense("tile_256x256x512_int", 256, 256, 512, A, B, OUT_FP32)
+    A = randint_matrix(256, 512, -2, 2, g, dtype)
+    B = randint_matrix(512, 256, -2, 2, g, dtype)
+    return Dense("tile_256x256x512_int", 256, 256, 512, A, B, OUT_FP32, dtype)
 
 
-def square_case(seed: int = 1002, n: int = 4096) -> Dense:
+def square_case(seed: int = 1002, n: int = 4096, dtype: str = "bf16") -> Dense:
     g = generator(seed)
-    A = normal_matrix(n, n, 1.0 / math.sqrt(n), g)
-    B = normal_matrix(n, n, 1.0 / math.sqrt(n), g)
-    return Dense("square_%d" % n, n, n, n, A, B, OUT_BF16)
+    A = normal_matrix(n, n, 1.0 / math.sqrt(n), g, dtype)
+    B = normal_matrix(n, n, 1.0 / math.sqrt(n), g, dtype)
+    return Dense("square_%d_%s" % (n, dtype), n, n, n, A, B, _out_for(dtype), dtype)
 
 
-def large_case(seed: int = 1003, n: int = 8192) -> Dense:
+def large_case(seed: int = 1003, n: int = 8192, dtype: str = "bf16") -> Dense:
     g = generator(seed)
-    A = uniform_matrix(n, n, -1.0, 1.0, g)
-    B = uniform_matrix(n, n, -1.0, 1.0, g)
-    return Dense("large_%d" % n, n, n, n, A, B, OUT_BF16)
+    A = uniform_matrix(n, n, -1.0, 1.0, g, dtype)
+    B = uniform_matrix(n, n, -1.0, 1.0, g, dtype)
+    return Dense("large_%d_%s" % (n, dtype), n, n, n, A, B, _out_for(dtype), dtype)
 
 
-def small_m_case(seed: int = 1004, M: int = 72, N: int = 16384, K: int = 7168) -> Dense:
+def small_m_case(seed: int = 1004, M: int = 72, N: int = 16384, K: int = 7168,
+                 dtype: str = "bf16") -> Dense:
     g = generator(seed)
-    A = normal_matrix(M, K, 0.02, g)
-    B = normal_matrix(K, N, 0.02, g)
-    return Dense("small_m_%dx%dx%d" % (M, N, K), M, N, K, A, B, OUT_BF16)
+    A = normal_matrix(M, K, 0.02, g, dtype)
+    B = normal_matrix(K, N, 0.02, g, dtype)
+    return Dense("small_m_%dx%dx%d_%s" % (M, N, K, dtype), M, N, K, A, B, _out_for(dtype), dtype)
 
 
 def grouped_case(seed: int = 1005, tokens: int = 4096, topk: int = 8, experts: int = 32,
-                 N: int = 4096, K: int = 4096) -> Grouped:
+                 N: int = 4096, K: int = 4096, dtype: str = "bf16") -> Grouped:
     g = generator(seed)
     counts = expert_counts(tokens, topk, experts, g)
     off = offsets_from_counts(counts)
-    A = normal_matrix(int(off[-1]), K, 1.0, g)
-    Bs = [normal_matrix(K, N, 0.02, g) for _ in range(experts)]
-    return Grouped("grouped_fc1_%dx%d_E%d" % (N, K, experts), N, K, A, Bs, off)
+    A = normal_matrix(int(off[-1]), K, 1.0, g, dtype)
+    Bs = [normal_matrix(K, N, 0.02, g, dtype) for _ in range(experts)]
+    return Grouped("grouped_fc1_%dx%d_E%d_%s" % (N, K, experts, dtype), N, K, A, Bs, off, dtype)
+
+
+def grouped_fc2_case(seed: int = 1006, tokens: int = 4096, topk: int = 8, experts: int = 32,
+                     N: int = 4096, K: int = 2048, dtype: str = "bf16") -> Grouped:
+    """Expert FC2 (down projection) over the FC1 case's token buckets: the
+    counts are drawn exactly as the FC1 case draws them (its seed, first draw),
+    the activations and weights from this case's own seed."""
+    counts = expert_counts(tokens, topk, experts, generator(1005))
+    off = offsets_from_counts(counts)
+    g = generator(seed)
+    A = normal_matrix(int(off[-1]), K, 1.0, g, dtype)
+    Bs = [normal_matrix(K, N, 0.02, g, dtype) for _ in range(experts)]
+    return Grouped("grouped_fc2_%dx%d_E%d_%s" % (N, K, experts, dtype), N, K, A, Bs, off, dtype)
 
 
 def case(index: int) -> Dense | Grouped:
-    """The five method workloads by index (1-based, as listed in the docstring)."""
-    return {1: tile_case, 2: square_case, 3: large_case, 4: small_m_case, 5: grouped_case}[index]()
+    """The method workloads by index (1-based, as listed in the docstring)."""
+    return {1: tile_case, 2: square_case, 3: large_case, 4: small_m_case, 5: grouped_case,
+            6: grouped_fc2_case}[index]()

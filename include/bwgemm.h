@@ -91,6 +91,34 @@ bwg_status grouped_gemm_fp16(const void* A, const void* const* B, void* D, const
                              int G, int M_total, int N, int K, void* stream);
 
 /*
+ * Grouped expert FC1 with the SwiGLU activation fused into the epilogue
+ * ("B200 的 2CTA 怎样调优", section 七, Gate/SwiGLU: y = up x SiLU(gate),
+ * with gate and up as column blocks of one GEMM, paired in the epilogue;
+ * "MegaMoE … 融合算子解读", section 09: FC1's accumulators go through SwiGLU
+ * in registers and only the activation is written).  For g in [0, G) and r in
+ * group g's rows:
+ *     gate = A[r, :] x B[g][:, 0 : N/2],   up = A[r, :] x B[g][:, N/2 : N]
+ *     H[r, j] = silu(gate_j) * up_j,       silu(x) = x / (1 + e^-x)
+ *   A, group_offsets, G, M_total, K: as for grouped_gemm_bf16.
+ *   B: HOST array of G device pointers, each [K, N] BF16 row-major (ldb = N),
+ *     the gate projection in columns 0 .. N/2-1, up in N/2 .. N-1.
+ *   H: device [M_total, N/2] BF16, dense (ldh = N/2); the gate/up product is
+ *     never written to memory.
+ *   N must be a multiple of 16 (the up block must start on a 16-byte
+ *   boundary), else BWG_ERR_ALIGNMENT.  Accumulation is FP32; silu and the
+ *   product are evaluated in FP32 and rounded once to BF16 (nearest even).
+ *   K = 0 writes zeros.  Errors as for grouped_gemm_bf16.
+ */
+bwg_status grouped_gemm_swiglu_bf16(const void* A, const void* const* B, void* H,
+                                    const int* group_offsets, int G, int M_total, int N, int K,
+                                    void* stream);
+
+/* Same as grouped_gemm_swiglu_bf16 with FP16 inputs and FP16 output. */
+bwg_status grouped_gemm_swiglu_fp16(const void* A, const void* const* B, void* H,
+                                    const int* group_offsets, int G, int M_total, int N, int K,
+                                    void* stream);
+
+/*
  * No-allocation form of gemm_bf16 for small M (M <= 128).  The pages have no
  * counterpart: it exists for callers that cannot let the library call
  * cudaMalloc -- code running while a stream is captured into a CUDA graph
@@ -189,6 +217,11 @@ typedef struct {
                               split in two along N (see bwg_tail_split) */
   int streamk;             /* SMALL_M: 1 if (tile, k-block) iterations are shared evenly
                               over all CTAs (partial tiles summed through a workspace) */
+  int workers;             /* CTA pairs (one-CTA kernel: CTAs) that run at once; the
+                              last-wave cut is computed for this many */
+  int dynamic;             /* 2CTA_2C: 1 if units are claimed at run time by cluster
+                              launch control (grid = 2 x units), 0 for the static
+                              persistent schedule (grid = 2 x workers) */
 } bwg_plan_info;
 
 /*

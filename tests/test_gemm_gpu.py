@@ -148,7 +148,7 @@ def _sample_indices(M, N, n, seed, tile_m=256, tile_n=256):
     I = list(rng.integers(0, M, n))
     J = list(rng.integers(0, N, n))
     # tile corners and edges
-    for m in sorted({0, 127, 128, 255, tile_m, M - 1, M // 2}):
+    for m in sorted({0, 127, 128, 255, tile_m, 511, 512, M - 1, M // 2}):
         for nn in sorted({0, 63, 64, 127, 128, 255, tile_n, N - 1}):
             if m < M and nn < N:
                 I.append(m)
@@ -187,6 +187,46 @@ def test_small_m_method_workload_full():
     D, _ = gpu_gemm(c.A, c.B, c.out_dtype)
     Dref, S = oracle.gemm(wl.bits(c.A), wl.bits(c.B))
     assert_within_bound(D, Dref, S, c.name)
+
+
+# FP16 inputs (FP16 output) on the method's dense workloads: the same draws
+# rounded to FP16; the oracle decodes the FP16 patterns.
+def test_fp16_square_4096_sampled():
+    c = wl.square_case(dtype="fp16")
+    D, _ = gpu_gemm(c.A, c.B, c.out_dtype)
+    assert D.dtype == torch.float16 and torch.isfinite(D.float()).all()
+    _check_sampled(c.A, c.B, D, 20000, 21, c.name)
+
+
+def test_fp16_large_8192_sampled():
+    c = wl.large_case(dtype="fp16")
+    D, _ = gpu_gemm(c.A, c.B, c.out_dtype)
+    assert torch.isfinite(D.float()).all()
+    _check_sampled(c.A, c.B, D, 20000, 22, c.name)
+    for r in (0, 511, 512, 8191):
+        Dref, S = oracle.gemm(wl.bits(c.A[r:r + 1]), wl.bits(c.B), "fp16")
+        assert_within_bound(D[r:r + 1], Dref, S, "fp16 row %d" % r)
+
+
+def test_fp16_small_m_method_workload_full():
+    c = wl.small_m_case(dtype="fp16")
+    D, _ = gpu_gemm(c.A, c.B, c.out_dtype)
+    Dref, S = oracle.gemm(wl.bits(c.A), wl.bits(c.B), "fp16")
+    assert_within_bound(D, Dref, S, c.name)
+
+
+@pytest.mark.parametrize("kind", ["2cta", "1cta", "2cta_2c", "small_m"])
+def test_fp16_integer_exact_every_kernel(kind):
+    """Integer FP16 inputs: exact on every kernel kind, FP32 and FP16 output."""
+    g = wl.generator(5500)
+    M = 72 if kind == "small_m" else 600
+    A = wl.randint_matrix(M, 320, -2, 2, g, "fp16")
+    B = wl.randint_matrix(320, 520, -2, 2, g, "fp16")
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B), "fp16")
+    D32, _ = gpu_gemm(A, B, wl.OUT_FP32, kind)
+    assert np.array_equal(D32.double().numpy(), Dref)
+    D16, _ = gpu_gemm(A, B, wl.OUT_FP16, kind)
+    assert_bits_equal(D16, oracle.round_to(Dref, "fp16"), "fp16 out " + kind)
 
 
 @pytest.mark.parametrize("kind", ["2cta", "1cta", "2cta_mc"])
@@ -343,3 +383,37 @@ def test_two_consumer_last_wave_quarters_exact(shape, monkeypatch):
     monkeypatch.setenv("BWG_NO_TAIL_SPLIT", "1")
     D2, _ = gpu_gemm(A, B, wl.OUT_FP32, "2cta_2c")
     assert np.array_equal(D2.double().numpy(), Dref)
+
+
+# ------------------------------------ cluster-launch-control scheduling ----
+
+@pytest.mark.parametrize("shape,no_split", [((4096, 4096, 64), "0"), ((2560, 4864, 128), "0"),
+                                            ((2560, 4864, 128), "1"), ((300, 520, 200), "0")])
+def test_dynamic_schedule_exact(shape, no_split, monkeypatch):
+    """Units claimed at run time (one pair launched per unit, running pairs
+    cancel pending ones and take their units): 128 units on 76 pairs, 95
+    tiles whose last wave is cut in quarters (or not), and a one-unit case."""
+    from blackwell_tensor_core_gb300 import ops
+    monkeypatch.setenv("BWG_SCHED", "clc")
+    monkeypatch.setenv("BWG_NO_TAIL_SPLIT", no_split)
+    M, N, K = shape
+    g = wl.generator(5600 + M)
+    A = wl.randint_matrix(M, K, -2, 2, g)
+    B = wl.randint_matrix(K, N, -2, 2, g)
+    pl = ops.plan(M, N, K, wl.OUT_FP32, force_kernel=ops.KERNEL_2CTA_2C)
+    assert pl.dynamic == 1 and pl.grid == 2 * pl.units
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+    D, _ = gpu_gemm(A, B, wl.OUT_FP32, "2cta_2c")
+    assert np.array_equal(D.double().numpy(), Dref)
+    D16, _ = gpu_gemm(A, B, wl.OUT_BF16, "2cta_2c")
+    assert_bits_equal(D16, oracle.round_to(Dref, "bf16"), "dynamic bf16 %s" % (shape,))
+
+
+def test_dynamic_schedule_8192_sampled(monkeypatch):
+    monkeypatch.setenv("BWG_SCHED", "clc")
+    c = wl.large_case()
+    D, _ = gpu_gemm(c.A, c.B, c.out_dtype, "2cta_2c")
+    _check_sampled(c.A, c.B, D, 8000, 16, c.name + " dynamic")
+    for r in (511, 512, 8191):
+        Dref, S = oracle.gemm(wl.bits(c.A[r:r + 1]), wl.bits(c.B))
+        assert_within_bound(D[r:r + 1], Dref, S, "row %d" % r)

@@ -83,24 +83,46 @@ def test_grouped_bad_offsets_are_reported_and_stay_in_bounds():
     assert_within_bound(D[:200], Dref0, S0, "group 0")
 
 
-def test_grouped_fc1_method_workload_sampled():
-    c = wl.grouped_case()
-    D, st, word = run_grouped(c.A, c.Bs, c.offsets)
-    assert st == 0, hex(word)
-    assert torch.isfinite(D.float()).all()
-    rng = np.random.default_rng(13)
+def _check_grouped_sampled(c, D, seed):
+    rng = np.random.default_rng(seed)
     Abits = wl.bits(c.A)
     for gi in range(c.G):
         r0, r1 = int(c.offsets[gi]), int(c.offsets[gi + 1])
         if r1 == r0:
             continue
-        rows = np.concatenate([[r0, r1 - 1, min(r0 + 255, r1 - 1), min(r0 + 256, r1 - 1)],
-                               rng.integers(r0, r1, 60)])
-        cols = np.concatenate([[0, 4095, 255, 256, 2047], rng.integers(0, c.N, 59)])
-        I = np.repeat(rows, 1)
-        J = cols[: len(rows)]
-        Dref, S = oracle.gemm_elements(Abits, wl.bits(c.Bs[gi]), I, J)
-        assert_within_bound(D[I, J], Dref, S, "expert %d" % gi)
+        seams = [r0, r1 - 1, r0 + 255, r0 + 256, r0 + 511, r0 + 512]
+        rows = np.concatenate([[min(r, r1 - 1) for r in seams], rng.integers(r0, r1, 58)])
+        cols = np.concatenate([[0, c.N - 1, 255, 256, c.N // 2, 127], rng.integers(0, c.N, 58)])
+        Dref, S = oracle.gemm_elements(Abits, wl.bits(c.Bs[gi]), rows, cols, c.in_dtype)
+        assert_within_bound(D[rows, cols], Dref, S, "%s expert %d" % (c.name, gi))
+
+
+def test_grouped_fc1_method_workload_sampled():
+    c = wl.grouped_case()
+    D, st, word = run_grouped(c.A, c.Bs, c.offsets)
+    assert st == 0, hex(word)
+    assert torch.isfinite(D.float()).all()
+    _check_grouped_sampled(c, D, 13)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_grouped_fc2_method_workload_sampled(dtype):
+    """Expert FC2 (down projection, K = 2048, N = 4096) over the FC1 case's
+    token buckets, with the same grouped kernel."""
+    c = wl.grouped_fc2_case(dtype=dtype)
+    assert np.array_equal(c.offsets, wl.grouped_case().offsets)
+    D, st, word = run_grouped(c.A, c.Bs, c.offsets)
+    assert st == 0, hex(word)
+    assert D.dtype == c.A.dtype and torch.isfinite(D.float()).all()
+    _check_grouped_sampled(c, D, 14)
+
+
+def test_grouped_fc1_fp16_sampled():
+    c = wl.grouped_case(dtype="fp16")
+    D, st, word = run_grouped(c.A, c.Bs, c.offsets)
+    assert st == 0, hex(word)
+    assert torch.isfinite(D.float()).all()
+    _check_grouped_sampled(c, D, 15)
 
 
 @pytest.mark.parametrize("counts", [[300, 0, 256, 1, 0, 511, 37], [16, 128, 129, 384, 100, 5]])
@@ -126,11 +148,13 @@ def test_grouped_swapped_group_ends_exact(counts, monkeypatch):
     assert_bits_equal(D2, want, "padded ends")
 
 
-@pytest.mark.parametrize("one_consumer", ["0", "1"])
-def test_grouped_both_kernels_exact(one_consumer, monkeypatch):
+@pytest.mark.parametrize("one_consumer,sched", [("0", "clc"), ("0", "static"), ("1", "static")])
+def test_grouped_both_kernels_exact(one_consumer, sched, monkeypatch):
     """Groups ending 1..511 rows into a 512-row unit (second consumer skipped
-    at 256 rows or fewer) and the 256-row kernel: both exact."""
+    at 256 rows or fewer), with dynamic and static scheduling, and the
+    256-row kernel: all exact."""
     monkeypatch.setenv("BWG_GROUPED_1C", one_consumer)
+    monkeypatch.setenv("BWG_SCHED", sched)
     counts = [1, 255, 256, 257, 511, 512, 513, 0, 700, 1030]
     off = wl.offsets_from_counts(counts)
     g = wl.generator(6300)
@@ -141,3 +165,32 @@ def test_grouped_both_kernels_exact(one_consumer, monkeypatch):
     D, st, word = run_grouped(A, Bs, off)
     assert st == 0, hex(word)
     assert_bits_equal(D, oracle.round_to(Dref, "bf16"), "grouped consumers=%s" % one_consumer)
+
+
+@pytest.mark.parametrize("swiglu", [False, True])
+def test_grouped_dynamic_schedule(swiglu, monkeypatch):
+    """Cluster-launch-control scheduling of the two-consumer grouped kernel:
+    115 units (more than the pairs that fit at once), ragged and empty
+    groups; exact without SwiGLU, within the SwiGLU bound with it."""
+    from blackwell_tensor_core_gb300 import ops
+    monkeypatch.setenv("BWG_SCHED", "clc")
+    counts = [1, 255, 256, 257, 511, 512, 513, 0, 700, 1030, 3000, 2048]
+    off = wl.offsets_from_counts(counts)
+    g = wl.generator(6500)
+    K, N = 64, 1040
+    A = wl.randint_matrix(int(off[-1]), K, -2, 2, g)
+    Bs = [wl.randint_matrix(K, N, -2, 2, g) for _ in counts]
+    dev = torch.device("cuda")
+    offd = torch.from_numpy(off).to(dev)
+    out = torch.full((A.shape[0], N // 2 if swiglu else N), float("nan"), dtype=A.dtype, device=dev)
+    ops.grouped_gemm(A.to(dev), [b.to(dev) for b in Bs], offd, out=out, swiglu=swiglu)
+    torch.cuda.synchronize()
+    st, word = ops.last_device_error()
+    assert st == 0, hex(word)
+    if swiglu:
+        Href, W = oracle.grouped_swiglu(wl.bits(A), [wl.bits(b) for b in Bs], off)
+        bad = oracle.bound_violations(out.cpu().double().numpy(), Href, W)
+        assert not bad.any(), "%d outside the SwiGLU bound" % bad.sum()
+    else:
+        Dref, _ = oracle.grouped_gemm(wl.bits(A), [wl.bits(b) for b in Bs], off)
+        assert_bits_equal(out.cpu(), oracle.round_to(Dref, "bf16"), "grouped dynamic")

@@ -37,10 +37,37 @@ def test_library_exports_every_declared_function(ops):
     header = re.sub(r"/\*.*?\*/", "", header, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w ]*?[\s\*]+(\w+)\s*\(", header, flags=re.M)
     names = [n for n in names if n not in ("if", "return")]
-    assert {"gemm_bf16", "gemm_fp16", "grouped_gemm_bf16", "bwg_last_device_error"} <= set(names)
+    assert {"gemm_bf16", "gemm_fp16", "grouped_gemm_bf16", "grouped_gemm_swiglu_bf16",
+            "grouped_gemm_swiglu_fp16", "bwg_last_device_error"} <= set(names)
     raw = ctypes.CDLL(ops.LIB_PATH)
     missing = [n for n in names if not hasattr(raw, n)]
     assert not missing, missing
+
+
+def test_swiglu_argument_checks_need_no_device(ops):
+    """Host-side checks of the SwiGLU entry point run before any CUDA call:
+    the up block must start on a 16-byte boundary (N a multiple of 16)."""
+    L = ops.lib()
+    arr = (ctypes.c_void_p * 1)(ctypes.c_void_p(256))
+    Bp = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+    assert L.grouped_gemm_swiglu_bf16(256, Bp, 256, 256, 1, 8, 24, 64, None) == 2
+    assert L.grouped_gemm_swiglu_fp16(256, Bp, 256, 256, 1, 8, 40, 64, None) == 2
+    assert L.grouped_gemm_swiglu_bf16(256, Bp, 256, 256, -1, 8, 32, 64, None) == 1
+    assert L.grouped_gemm_swiglu_bf16(256, Bp, 264, 256, 1, 8, 32, 64, None) == 2  # H misaligned
+    assert L.grouped_gemm_swiglu_bf16(256, Bp, 256, 256, 0, 8, 32, 64, None) == 0  # nothing to do
+
+
+def test_dynamic_schedule_plan(ops, monkeypatch):
+    """BWG_SCHED=clc: the two-consumer plan launches one pair per unit; the
+    last-wave cut is still computed for the pairs that run at once."""
+    static = ops.plan(8192, 8192, 8192, force_kernel=ops.KERNEL_2CTA_2C)
+    assert static.dynamic == 0 and static.workers == 76 and static.grid == 152
+    monkeypatch.setenv("BWG_SCHED", "clc")
+    dyn = ops.plan(8192, 8192, 8192, force_kernel=ops.KERNEL_2CTA_2C)
+    assert dyn.dynamic == 1 and dyn.workers == 76
+    assert dyn.units == static.units and dyn.grid == 2 * dyn.units
+    # other kernels keep the static schedule
+    assert ops.plan(8192, 8192, 8192, force_kernel=ops.KERNEL_2CTA).dynamic == 0
 
 
 def test_status_strings(ops):

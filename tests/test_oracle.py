@@ -236,3 +236,8 @@ def test_workload_generators_are_seeded_and_shaped():
     assert set(torch.unique(c1.A.float()).tolist()) <= {-2.0, -1.0, 0.0, 1.0, 2.0}
     counts = wl.expert_counts(4096, 8, 32, wl.generator(1005))
     assert counts.sum() == 32768 and len(counts) == 32
+    # FC2 runs over the FC1 case's token buckets
+    fc1 = wl.grouped_case(experts=4, N=16, K=16)
+    fc2 = wl.grouped_fc2_case(experts=4, N=16, K=16)
+    assert np.array_equal(fc1.offsets, fc2.offsets) and fc2.A.shape == (fc1.total, 16)
+    assert wl.square_case(n=64, dtype="fp16").A.dtype == torch.float16

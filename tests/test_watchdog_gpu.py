@@ -22,11 +22,13 @@ def _built():
     build.build()
 
 
-@pytest.mark.parametrize("kind,M", [("2cta", 256), ("1cta", 256), ("2cta_mc", 512), ("2cta_2c", 512),
-                                    (None, 64)])
-def test_stalled_stage_barrier_times_out_and_context_survives(kind, M):
+@pytest.mark.parametrize("kind,M,sched", [("2cta", 256, "static"), ("1cta", 256, "static"),
+                                          ("2cta_mc", 512, "static"), ("2cta_2c", 512, "static"),
+                                          ("2cta_2c", 512, "clc"), (None, 64, "static")])
+def test_stalled_stage_barrier_times_out_and_context_survives(kind, M, sched, monkeypatch):
     from blackwell_tensor_core_gb300 import ops
     from gpu_util import forced_kernel
+    monkeypatch.setenv("BWG_SCHED", sched)
     g = wl.generator(7000)
     A = wl.randint_matrix(M, 256, -2, 2, g)
     B = wl.randint_matrix(256, 256, -2, 2, g)
@@ -48,3 +50,34 @@ def test_stalled_stage_barrier_times_out_and_context_survives(kind, M):
     Dg, _ = gpu_gemm(A, B, wl.OUT_FP32, kind)
     Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
     assert np.array_equal(Dg.double().numpy(), Dref)
+
+
+@pytest.mark.parametrize("sched", ["clc", "static"])
+def test_grouped_stalled_stage_barrier_times_out(sched, monkeypatch):
+    """The grouped two-consumer kernel (dynamic and static scheduling) gives
+    up on a stage barrier that cannot complete, reports BWG_ERR_TIMEOUT, and
+    the next call is exact."""
+    from blackwell_tensor_core_gb300 import ops
+    monkeypatch.setenv("BWG_SCHED", sched)
+    counts = [300, 700]
+    off = wl.offsets_from_counts(counts)
+    g = wl.generator(7100)
+    A = wl.randint_matrix(int(off[-1]), 128, -2, 2, g)
+    Bs = [wl.randint_matrix(128, 256, -2, 2, g) for _ in counts]
+    dev = torch.device("cuda")
+    Ad, Bd, offd = A.to(dev), [b.to(dev) for b in Bs], torch.from_numpy(off).to(dev)
+    D = torch.zeros((A.shape[0], 256), dtype=torch.bfloat16, device=dev)
+    ops.set_watchdog_ns(50_000_000)
+    ops.debug_set_tx_extra(1024)
+    try:
+        ops.grouped_gemm(Ad, Bd, offd, out=D)
+        st, word = ops.last_device_error()
+    finally:
+        ops.debug_set_tx_extra(0)
+        ops.set_watchdog_ns(0)
+    assert st == 5 and (word >> 56) == 1, (st, hex(word))
+    ops.grouped_gemm(Ad, Bd, offd, out=D)
+    st, word = ops.last_device_error()
+    assert st == 0, hex(word)
+    Dref, _ = oracle.grouped_gemm(wl.bits(A), [wl.bits(b) for b in Bs], off)
+    assert np.array_equal(wl.bits(D.cpu()), oracle.round_to(Dref, "bf16"))
