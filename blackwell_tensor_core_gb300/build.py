@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libbwgemm.so")
-SOURCES = ["api.cu", "gemm_tc.cu", "gemm_small_m.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "gemm_small_m.cu", "probes.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -61,6 +61,12 @@ struct DeviceState {
   int clusters_grouped_2c = 0;
   int ctas_1cta = 0;
   int clusters_grouped = 0;
+  // host-buffer entry point: copy streams and chunk events, made on first use
+  bool host_ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_done = nullptr;
+  cudaEvent_t ev_in[8] = {}, ev_out[8] = {};
+  std::mutex host_mu;  // one host-buffer call at a time per device enqueues
 };
 
 std::mutex g_mu;
@@ -842,6 +848,10 @@ bwg_status gemm_bf16_small_m_noalloc(const void* A, const void* B, void* D, int 
                              static_cast<cudaStream_t>(stream));
 }
 
+// Host-buffer product, pipelined over row chunks of A and D: B and the first
+// chunk of A go up first; then chunk c's product runs on `stream` while chunk
+// c+1 is copied in on one copy stream and chunk c-1's result goes back on the
+// other, so the two copy directions and the tensor cores work at once.
 bwg_status gemm_bf16_host(const void* A_host, const void* B_host, void* D_host, int M, int N, int K,
                           int out_dtype, void* dA, void* dB, void* dD, void* stream) {
   if (M < 0 || N < 0 || K < 0) return BWG_ERR_INVALID_ARG;
@@ -849,15 +859,62 @@ bwg_status gemm_bf16_host(const void* A_host, const void* B_host, void* D_host, 
     return BWG_ERR_INVALID_ARG;
   bwg_status s = check_args(dA, dB, dD, M, N, K, K, N, N, out_dtype);
   if (s != BWG_OK || M == 0 || N == 0) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t a_bytes = static_cast<size_t>(M) * K * 2, b_bytes = static_cast<size_t>(K) * N * 2;
-  const size_t d_bytes = static_cast<size_t>(M) * N * out_elt(out_dtype);
-  if (K > 0 && (cudaMemcpyAsync(dA, A_host, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-                cudaMemcpyAsync(dB, B_host, b_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess))
-    return launch_status(cudaErrorUnknown);
-  s = run_dense(false, dA, dB, dD, M, N, K, K, N, N, out_dtype, st);
-  if (s != BWG_OK) return s;
-  return launch_status(cudaMemcpyAsync(D_host, dD, d_bytes, cudaMemcpyDeviceToHost, st));
+  DeviceState* st = nullptr;
+  if ((s = ensure_device(&st)) != BWG_OK) return s;
+  cudaStream_t us = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(st->host_mu);
+  if (!st->host_ready) {
+    bool ok = cudaStreamCreateWithFlags(&st->h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&st->d2h, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&st->ev_start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&st->ev_done, cudaEventDisableTiming) == cudaSuccess;
+    for (int c = 0; ok && c < 8; ++c)
+      ok = cudaEventCreateWithFlags(&st->ev_in[c], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&st->ev_out[c], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) return launch_status(cudaErrorUnknown);
+    st->host_ready = true;
+  }
+  // Chunks of whole 512-row tiles, at most 8, at least 1024 rows each.
+  const int want = std::max(1, std::min(8, M / 1024));
+  const int rows = ceil_div(ceil_div(M, want), 512) * 512;
+  const int chunks = ceil_div(M, rows);
+  const size_t oe = static_cast<size_t>(out_elt(out_dtype));
+  auto a_at = [&](const void* base, int r) {
+    return static_cast<const uint8_t*>(base) + static_cast<size_t>(r) * K * 2;
+  };
+  auto d_at = [&](void* base, int r) {
+    return static_cast<uint8_t*>(base) + static_cast<size_t>(r) * N * oe;
+  };
+  auto fail = [&](cudaError_t e) { return e == cudaSuccess ? BWG_OK : launch_status(e); };
+  // nothing starts before the work already on the caller's stream
+  cudaError_t e = cudaEventRecord(st->ev_start, us);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st->h2d, st->ev_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st->d2h, st->ev_start, 0);
+  if (e == cudaSuccess && K > 0)
+    e = cudaMemcpyAsync(dB, B_host, static_cast<size_t>(K) * N * 2, cudaMemcpyHostToDevice, st->h2d);
+  for (int c = 0; e == cudaSuccess && c < chunks; ++c) {
+    const int r0 = c * rows, rc = std::min(rows, M - r0);
+    if (K > 0)
+      e = cudaMemcpyAsync(const_cast<uint8_t*>(a_at(dA, r0)), a_at(A_host, r0),
+                          static_cast<size_t>(rc) * K * 2, cudaMemcpyHostToDevice, st->h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(st->ev_in[c], st->h2d);
+  }
+  for (int c = 0; e == cudaSuccess && c < chunks; ++c) {
+    const int r0 = c * rows, rc = std::min(rows, M - r0);
+    e = cudaStreamWaitEvent(us, st->ev_in[c], 0);
+    if (e != cudaSuccess) break;
+    s = run_dense(false, a_at(dA, r0), dB, d_at(dD, r0), rc, N, K, K, N, N, out_dtype, us);
+    if (s != BWG_OK) return s;
+    e = cudaEventRecord(st->ev_out[c], us);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st->d2h, st->ev_out[c], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(d_at(D_host, r0), d_at(dD, r0), static_cast<size_t>(rc) * N * oe,
+                          cudaMemcpyDeviceToHost, st->d2h);
+  }
+  // the caller's stream finishes after the last copy back
+  if (e == cudaSuccess) e = cudaEventRecord(st->ev_done, st->d2h);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(us, st->ev_done, 0);
+  return fail(e);
 }
 
 const char* bwg_status_string(int status) {
@@ -891,6 +948,49 @@ bwg_status bwg_last_device_error(void* stream, unsigned long long* info) {
   if (kind == kFaultTimeout) return BWG_ERR_TIMEOUT;
   if (kind == kFaultBadOffsets) return BWG_ERR_INVALID_ARG;
   return BWG_OK;
+}
+
+bwg_status bwg_probe_cluster_pair(const float* in, float* sum_out, int* peer_out, int n,
+                                  void* stream) {
+  if (n <= 0 || (n & 1) || n > 65534 || in == nullptr || sum_out == nullptr || peer_out == nullptr)
+    return BWG_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  bwg_status s = ensure_device(&st);
+  if (s != BWG_OK) return s;
+  return launch_status(
+      launch_probe_cluster_pair(in, sum_out, peer_out, n, static_cast<cudaStream_t>(stream)));
+}
+
+bwg_status bwg_probe_tma_swizzle(const void* src, void* out, void* stream) {
+  if (src == nullptr || out == nullptr) return BWG_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(out)) return BWG_ERR_ALIGNMENT;
+  DeviceState* st = nullptr;
+  bwg_status s = ensure_device(&st);
+  if (s != BWG_OK) return s;
+  CUtensorMap map;
+  if (!encode_map_direct(&map, src, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64, 64, 128, 64, 64,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+    return BWG_ERR_CUDA;
+  return launch_status(launch_probe_tma_swizzle(map, out, st->err, g_timeout_ns.load(),
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+bwg_status bwg_probe_mma(const void* A, const void* B, float* D, int k_steps, int fp16,
+                         void* stream) {
+  if (A == nullptr || B == nullptr || D == nullptr || k_steps < 1 || k_steps > 4)
+    return BWG_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D)) return BWG_ERR_ALIGNMENT;
+  DeviceState* st = nullptr;
+  bwg_status s = ensure_device(&st);
+  if (s != BWG_OK) return s;
+  const CUtensorMapDataType t = fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap ma, mb;
+  if (!encode_map_direct(&ma, A, t, 64, 128, 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_map_direct(&mb, B, t, 256, 64, 512, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return BWG_ERR_CUDA;
+  const uint32_t idesc = make_idesc_f16(fp16 ? kFmtF16 : kFmtBF16, false, true, 128, 256);
+  return launch_status(launch_probe_mma(ma, mb, D, k_steps, idesc, st->err, g_timeout_ns.load(),
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 void bwg_set_watchdog_ns(unsigned long long ns) { g_timeout_ns.store(ns ? ns : 2000000000ull); }

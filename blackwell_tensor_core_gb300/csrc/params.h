@@ -96,6 +96,15 @@ cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, c
 cudaError_t launch_small_m(const SmallMParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_zero_fill(void* d, int rows, int cols, int ld, int elt_bytes, cudaStream_t s);
 
+// Probe kernels (test hooks, probes.cu).
+cudaError_t launch_probe_cluster_pair(const float* in, float* sum_out, int* peer_out, int n,
+                                      cudaStream_t s);
+cudaError_t launch_probe_tma_swizzle(const CUtensorMap& map, void* out, unsigned long long* err,
+                                     unsigned long long timeout_ns, cudaStream_t s);
+cudaError_t launch_probe_mma(const CUtensorMap& map_a, const CUtensorMap& map_b, float* d, int k_steps,
+                             uint32_t idesc, unsigned long long* err, unsigned long long timeout_ns,
+                             cudaStream_t s);
+
 // Occupancy helpers: co-resident clusters (or CTAs) for a given launch shape.
 int max_active_clusters_gemm(int cluster, bool grouped, size_t smem);
 int max_active_ctas_small_m(size_t smem);

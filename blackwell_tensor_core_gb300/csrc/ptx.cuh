@@ -262,6 +262,14 @@ BWG_DEV uint32_t ld_shared_u32(uint32_t addr) {
   return v;
 }
 
+// Load from the shared::cluster window (own or a peer CTA's shared memory,
+// an address from mapa_shared).
+BWG_DEV uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------- conversion ----
 
 // Round-to-nearest-even packs: low 16 bits <- lo, high 16 bits <- hi.

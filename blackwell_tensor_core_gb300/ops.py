@@ -72,6 +72,12 @@ def lib() -> ctypes.CDLL:
             L.bwg_status_string.restype = ctypes.c_char_p
             L.bwg_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_ulonglong)]
             L.bwg_last_device_error.restype = i
+            for name, args in (("bwg_probe_cluster_pair", [vp, vp, vp, i, vp]),
+                               ("bwg_probe_tma_swizzle", [vp, vp, vp]),
+                               ("bwg_probe_mma", [vp, vp, vp, i, i, vp])):
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = i
             L.bwg_set_watchdog_ns.argtypes = [ctypes.c_ulonglong]
             L.bwg_set_watchdog_ns.restype = None
             L.bwg_debug_set_tx_extra.argtypes = [ctypes.c_uint]
@@ -226,7 +232,8 @@ def grouped_gemm_fp16(A_ptr: int, B_ptrs: list, D_ptr: int, offsets_ptr: int, G:
 
 def gemm_bf16_host(A_host: torch.Tensor, B_host: torch.Tensor, D_host: torch.Tensor,
                    dA: torch.Tensor, dB: torch.Tensor, dD: torch.Tensor, stream=None) -> None:
-    """Host-buffer form: copies in, multiplies, copies out, all on `stream`."""
+    """Host-buffer form: copies in, multiplies, copies out; `stream` completes
+    after the last copy back (the library pipelines over row chunks)."""
     M, K = A_host.shape
     N = B_host.shape[1]
     if D_host.dtype not in _OUT_CODES:

@@ -147,11 +147,19 @@ bwg_status gemm_bf16_small_m_noalloc(const void* A, const void* B, void* D, int 
 
 /*
  * End-to-end convenience form of gemm_bf16 for host-resident data: copies
- * A_host [M,K] and B_host [K,N] (dense, BF16, preferably pinned) into the
- * caller's device buffers dA, dB, runs the product into dD ([M,N], out_dtype)
- * and copies dD back to D_host, all enqueued on `stream` in that order.  The
- * library allocates nothing; the caller synchronises the stream before
- * reading D_host.
+ * A_host [M,K] and B_host [K,N] (dense, BF16, pinned for the copies to run
+ * asynchronously) into the caller's device buffers dA, dB, runs the product
+ * into dD ([M,N], out_dtype) and copies dD back to D_host.  The work is
+ * pipelined over up to 8 row chunks of A and D (whole 512-row tiles, at
+ * least 1024 rows): B and A's chunks are copied in on one internal stream,
+ * each chunk's product runs on `stream` once its rows have arrived, and its
+ * result is copied back on a second internal stream while the next chunk
+ * computes.  Everything starts after the work already queued on `stream`,
+ * and `stream` completes only after the last copy back, so the caller
+ * synchronises `stream` before reading D_host.  The internal streams and
+ * events are made on a device's first call and kept; calls from several
+ * host threads on one device are serialised while they enqueue.  The
+ * library allocates no device memory.
  */
 bwg_status gemm_bf16_host(const void* A_host, const void* B_host, void* D_host, int M, int N, int K,
                           int out_dtype, void* dA, void* dB, void* dD, void* stream);
@@ -177,6 +185,32 @@ bwg_status bwg_last_device_error(void* stream, unsigned long long* info);
  * kernel unwinds instead of hanging.
  */
 void bwg_set_watchdog_ns(unsigned long long ns);
+
+/*
+ * Probes: small kernels that check one mechanism each, for the tests.  None
+ * is on the GEMM path.  All pointers are device pointers; errors as usual,
+ * and a wait that times out is reported by bwg_last_device_error.
+ *
+ * bwg_probe_cluster_pair: n (even) CTAs in clusters of 2; CTA i writes
+ *   peer_out[i] = index of its cluster peer and sum_out[i] = in[i] + in[peer],
+ *   read from the peer's shared memory (mapa + ld.shared::cluster).  The
+ *   pages print [1, 0, 3, 2] for the peer indices of 4 CTAs ("B200 的 2CTA
+ *   怎样调优", Cluster section) and [1, 1, 5, 5, 9, 9, 13, 13] for the sums
+ *   of inputs 0..7 ("从 CUDA 代码到 GPU 执行", pair_sum).
+ * bwg_probe_tma_swizzle: one TMA load of the 64 x 64 16-bit tile `src`
+ *   (row-major, 128-byte rows) with 128-byte swizzle; `out` receives the 8 KiB
+ *   shared-memory image ("GEMM优化（三）" section 2.1: 16-byte chunk c of row r
+ *   lands at r * 128 + ((c ^ (r % 8)) * 16)).
+ * bwg_probe_mma: D [128, 256] FP32 = A[:, 0:16k] x B[0:16k, :] for
+ *   k = k_steps (1..4) tcgen05.mma instructions of K = 16, with A [128, 64]
+ *   and B [64, 256] row-major BF16 (fp16 = 0) or FP16 (fp16 = 1), loaded by
+ *   TMA and read back from TMEM, with the GEMM kernels' descriptors.
+ */
+bwg_status bwg_probe_cluster_pair(const float* in, float* sum_out, int* peer_out, int n,
+                                  void* stream);
+bwg_status bwg_probe_tma_swizzle(const void* src, void* out, void* stream);
+bwg_status bwg_probe_mma(const void* A, const void* B, float* D, int k_steps, int fp16,
+                         void* stream);
 
 /*
  * Test hook: adds `bytes` to the transaction count every stage expects, so

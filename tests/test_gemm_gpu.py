@@ -417,3 +417,56 @@ def test_dynamic_schedule_8192_sampled(monkeypatch):
     for r in (511, 512, 8191):
         Dref, S = oracle.gemm(wl.bits(c.A[r:r + 1]), wl.bits(c.B))
         assert_within_bound(D[r:r + 1], Dref, S, "row %d" % r)
+
+
+# ------------------------------------------------- host-buffer entry point --
+
+def _host_call(A, B, out_dtype, dA=None, dB=None, dD=None):
+    from blackwell_tensor_core_gb300 import ops
+    M, K = A.shape
+    N = B.shape[1]
+    hA, hB = A.pin_memory(), B.pin_memory()
+    hD = torch.full((M, N), float("nan"), dtype=OUT_TORCH[out_dtype]).pin_memory()
+    dA = dA if dA is not None else torch.empty((M, K), dtype=A.dtype, device="cuda")
+    dB = dB if dB is not None else torch.empty((K, N), dtype=B.dtype, device="cuda")
+    dD = dD if dD is not None else torch.empty((M, N), dtype=OUT_TORCH[out_dtype], device="cuda")
+    ops.gemm_bf16_host(hA, hB, hD, dA, dB, dD)
+    return hD, (dA, dB, dD)
+
+
+@pytest.mark.parametrize("M", [700, 3000, 9000])
+def test_host_entry_point_pipelined_chunks_exact(M):
+    """1, 2 and 6 row chunks (whole 512-row tiles, a ragged last chunk): the
+    copies, products and copies back are ordered by events; exact result."""
+    g = wl.generator(5700 + M)
+    A = wl.randint_matrix(M, 192, -2, 2, g)
+    B = wl.randint_matrix(192, 264, -2, 2, g)
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+    hD, _ = _host_call(A, B, wl.OUT_FP32)
+    torch.cuda.current_stream().synchronize()
+    assert np.array_equal(hD.double().numpy(), Dref)
+
+
+def test_host_entry_point_back_to_back_calls_reuse_buffers():
+    """Two calls on one stream with the same device buffers and different
+    inputs: the second call's copies wait for the first call's products, and
+    each host result is that call's own product."""
+    g = wl.generator(5800)
+    A1 = wl.randint_matrix(4096, 128, -2, 2, g)
+    B1 = wl.randint_matrix(128, 1024, -2, 2, g)
+    A2 = wl.randint_matrix(4096, 128, -2, 2, g)
+    B2 = wl.randint_matrix(128, 1024, -2, 2, g)
+    h1, bufs = _host_call(A1, B1, wl.OUT_BF16)
+    h2, _ = _host_call(A2, B2, wl.OUT_BF16, *bufs)
+    torch.cuda.current_stream().synchronize()
+    for A, B, h in ((A1, B1, h1), (A2, B2, h2)):
+        Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+        assert_bits_equal(h, oracle.round_to(Dref, "bf16"), "host call")
+
+
+def test_host_entry_point_8192_sampled():
+    """The end-to-end configuration the benchmark times (8192^3, BF16 out)."""
+    c = wl.large_case()
+    hD, _ = _host_call(c.A, c.B, c.out_dtype)
+    torch.cuda.current_stream().synchronize()
+    _check_sampled(c.A, c.B, hD, 8000, 17, c.name + " host entry")
