@@ -81,8 +81,9 @@ def test_single_tile_mma_exact(k_steps, dtype):
     g = wl.generator(8000 + k_steps)
     A = wl.randint_matrix(128, 64, -2, 2, g, dtype)
     B = wl.randint_matrix(64, 256, -2, 2, g, dtype)
+    Ad, Bd = A.cuda(), B.cuda()  # kept alive until the probe has run
     D = torch.full((128, 256), float("nan"), dtype=torch.float32, device="cuda")
-    _check(ops.lib().bwg_probe_mma(A.cuda().data_ptr(), B.cuda().data_ptr(), D.data_ptr(), k_steps,
+    _check(ops.lib().bwg_probe_mma(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), k_steps,
                                    1 if dtype == "fp16" else 0, _stream()))
     K = 16 * k_steps
     Dref, _ = oracle.gemm(wl.bits(A[:, :K].contiguous()), wl.bits(B[:K].contiguous()), dtype)
