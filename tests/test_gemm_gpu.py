@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from blackwell_tensor_core_gb300 import workloads as wl
-from gpu_util import assert_bits_equal, assert_within_bound, gpu_gemm, in_dtype_name
+from gpu_util import OUT_TORCH, assert_bits_equal, assert_within_bound, gpu_gemm, in_dtype_name
 
 pytestmark = pytest.mark.gpu
 
