@@ -44,6 +44,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<unsigned> g_tx_extra{0};
+std::atomic<unsigned long long*> g_trace{nullptr};  // unit trace buffer (dense and grouped pair kernels)
 
 constexpr int kMaxDevices = 64;
 constexpr int kBarrierArea = 2048;  // barriers, TMEM address slot, grouped tables
@@ -139,6 +140,20 @@ bwg_status get_workspace(cudaStream_t stream, size_t ws_bytes, int n_counters, W
 }
 
 // Most CTAs that share one tile under the stream-K split.
+// Zero every stream-K arrival counter of this device (after a timeout).
+bwg_status clear_workspace_counters() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (auto& kv : g_workspaces) {
+    if (static_cast<int>(kv.first >> 56) != dev || kv.second.counters == nullptr) continue;
+    if (cudaMemset(kv.second.counters, 0, static_cast<size_t>(kv.second.n_counters) * sizeof(int)) !=
+        cudaSuccess)
+      return BWG_ERR_CUDA;
+  }
+  return BWG_OK;
+}
+
 int streamk_max_sharers(int tiles, int kb, int grid) {
   const long long W = static_cast<long long>(tiles) * kb;
   int most = 1;
@@ -324,6 +339,32 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     if (two && dynamic_sched_from_env(false)) {
       o->dynamic = 1;
       o->grid = 2 * o->units;  // one pair per unit; running pairs claim the rest
+    } else if (two) {
+      // stream-K last wave, if it beats the (cut or uncut) last wave; it
+      // spreads over every pair that fits, also when there are fewer tiles
+      const int C = max_clusters_2c > 0 ? max_clusters_2c : sm_count / 2;
+      const int cut_cost =
+          R == 0 ? 1000 : ceil_div(f * R, o->workers) * (f == 2 ? kCostHalf2 : kCostQuarter2);
+      // Opt-in (BWG_STREAMK_DENSE=1 takes it whenever it applies): measured
+      // on GB300 it does not pay.  Pairs working at unrelated k offsets of
+      // different tiles share no A or B data in L2, so the stream-K phase is
+      // DRAM-bound at about 1.6x the per-k-block time of the lock-stepped
+      // whole-tile waves, which cancels the better balance (4096^3: 94.8 vs
+      // 92.8 us; 4096^2 x 16384: 339 vs 308 us).
+      const char* env = std::getenv("BWG_STREAMK_DENSE");
+      int segs = 0;
+      int sk = 0;
+      if (env != nullptr && env[0] == '1')
+        sk = streamk_tiles(base_units, C, o->k_blocks, 1 << 30, &segs);
+      (void)cut_cost;
+      if (sk > 0) {
+        o->streamk = 1;
+        o->sk_tiles = sk;
+        o->sk_segs = segs;
+        o->workers = C;
+        o->grid = 2 * C;
+        o->units = segs * C + base_units - sk;
+      }
     }
   } else {
     o->workers = o->grid;
@@ -569,6 +610,7 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
   p.out_dtype = out_dtype;
   p.idesc = pl.idesc;
   p.tx_extra = g_tx_extra.load();
+  p.trace = g_trace.load();
   p.no_tail_split = no_tail_split_from_env();
   p.direct_store = direct_store_from_env() ? 1 : 0;
   if (pl.kernel == BWG_KERNEL_2CTA)
@@ -576,6 +618,17 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
   if (pl.kernel == BWG_KERNEL_2CTA_MC)
     return launch_status(launch_gemm_2cta_mc(p, pl.grid, pl.smem_total, stream));
   p.workers = pl.workers;
+  if (pl.kernel == BWG_KERNEL_2CTA_2C && pl.streamk) {
+    p.sk_tiles = pl.sk_tiles;
+    p.sk_segs = pl.sk_segs;
+    p.ws_slots = streamk_max_sharers(pl.sk_tiles, pl.k_blocks, pl.workers);
+    const size_t ws_bytes = static_cast<size_t>(pl.sk_tiles) * p.ws_slots * 16u * 32u * kTileN * 4u;
+    Workspace w;
+    bwg_status ws = get_workspace(stream, ws_bytes, pl.sk_tiles * 16, &w);
+    if (ws != BWG_OK) return ws;
+    p.ws = w.ws;
+    p.ws_counters = w.counters;
+  }
   if (pl.kernel == BWG_KERNEL_2CTA_2C)
     return launch_status(launch_gemm_2cta_2c(p, pl.grid, pl.smem_total, stream, pl.dynamic != 0));
   return launch_status(launch_gemm_1cta(p, pl.grid, pl.smem_total, stream));
@@ -648,6 +701,7 @@ bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
     p.out_dtype = fp16 ? BWG_OUT_FP16 : BWG_OUT_BF16;
     p.idesc = make_idesc_f16(fp16 ? kFmtF16 : kFmtBF16, false, true, 2 * kRowsPerCta, kTileN);
     p.tx_extra = g_tx_extra.load();
+    p.trace = g_trace.load();
     p.G = gn;
     p.g_begin = g0;
     p.G_total = G;
@@ -945,7 +999,12 @@ bwg_status bwg_last_device_error(void* stream, unsigned long long* info) {
     return launch_status(cudaErrorUnknown);
   *info = w;
   const unsigned long long kind = w >> 56;
-  if (kind == kFaultTimeout) return BWG_ERR_TIMEOUT;
+  if (kind == kFaultTimeout) {
+    // A kernel that gave up may have left stream-K arrival counters behind;
+    // they must read zero at the start of every call.
+    if (clear_workspace_counters() != BWG_OK) return BWG_ERR_CUDA;
+    return BWG_ERR_TIMEOUT;
+  }
   if (kind == kFaultBadOffsets) return BWG_ERR_INVALID_ARG;
   return BWG_OK;
 }
@@ -997,6 +1056,8 @@ void bwg_set_watchdog_ns(unsigned long long ns) { g_timeout_ns.store(ns ? ns : 2
 
 void bwg_debug_set_tx_extra(unsigned int bytes) { g_tx_extra.store(bytes); }
 
+void bwg_debug_set_trace(void* buffer) { g_trace.store(static_cast<unsigned long long*>(buffer)); }
+
 bwg_status bwg_plan(int M, int N, int K, int out_dtype, int sm_count, int force_kernel,
                     int force_stages, bwg_plan_info* out) {
   if (out == nullptr || M < 0 || N < 0 || K < 0 || sm_count <= 0) return BWG_ERR_INVALID_ARG;
@@ -1043,6 +1104,10 @@ int bwg_tail_split(int T, int C) { return tail_split_count(T, C); }
 
 int bwg_tail_split_f(int T, int C, int max_f, int* f) {
   return tail_split(T, C, max_f, max_f == 4 ? kCostHalf2 : kCostHalf1, kCostQuarter2, f);
+}
+
+int bwg_streamk_tiles(int T, int C, int kb, int cut_cost, int* segs) {
+  return streamk_tiles(T, C, kb, cut_cost, segs);
 }
 
 void bwg_unit_part(int u, int T, int R, int f, int* tile, int* part, int* parts) {

@@ -73,6 +73,8 @@ struct Tile {
   int g;
   int swap_rows;  // > 0: rows m0 .. m0+swap_rows-1 computed with swapped operands
   int cmask;      // MMA consumers with work in this unit (bit c: rows m0 + 256c ..)
+  int kb0, kb1;   // k-blocks of the unit (all of K except for stream-K segments)
+  int sk;         // stream-K tile index (0 .. sk_tiles-1), or -1
 };
 
 // MC pairs per cluster (1, or 2 when the pairs share B through TMA multicast):
@@ -80,7 +82,7 @@ struct Tile {
 // and pair `pair` of the cluster takes tile row (unit row * MC + pair).
 // SW (fused SwiGLU): a tile's 256 MMA columns are 128 gate and 128 up
 // columns, so it covers 128 output columns; n0 counts output columns.
-template <int CG, int MC, bool GROUPED, int NC = 1, bool SW = false>
+template <int CG, int MC, bool GROUPED, int NC = 1, bool SW = false, bool DYN = false>
 struct Sched {
   static constexpr int kTileM = kRowsPerCta * CG * NC;
   static constexpr int kOutCols = SW ? kTileN / 2 : kTileN;  // output columns of a whole tile
@@ -93,25 +95,90 @@ struct Sched {
   int tiles;          // whole tiles
   int split;          // tiles of the last wave that are cut
   int f;              // parts per cut tile (2 halves, or 4 quarters with two consumers)
+  int workers;        // pairs (or CTAs) that run at once
+  int sk_units;       // stream-K segment units before the data-parallel tiles
+  long long sk_iters; // stream-K (tile, k-block) iterations
 
   __device__ Sched(const GemmParams& p_, const int* prefix_, const int* lo_, const int* hi_,
                    int workers, int pair_)
-      : p(p_), prefix(prefix_), lo(lo_), hi(hi_), pair(pair_) {
+      : p(p_), prefix(prefix_), lo(lo_), hi(hi_), pair(pair_), workers(workers) {
     rows_of_units = (p.num_m_tiles + MC - 1) / MC;
     if constexpr (GROUPED)
       tiles = prefix[p.G];
     else
       tiles = rows_of_units * p.num_n_tiles;
     f = 1;
-    split = p.no_tail_split ? 0
-                            : tail_split(tiles, workers, NC == 2 ? 4 : 2,
-                                         NC == 2 ? kCostHalf2 : kCostHalf1, kCostQuarter2, &f);
+    sk_units = 0;
+    sk_iters = 0;
+    if (kStreamK && p.sk_tiles > 0) {
+      // stream-K replaces the last-wave cut
+      split = 0;
+      sk_units = p.sk_segs * workers;
+      sk_iters = static_cast<long long>(p.sk_tiles) * p.num_k_blocks;
+    } else {
+      split = p.no_tail_split ? 0
+                              : tail_split(tiles, workers, NC == 2 ? 4 : 2,
+                                           NC == 2 ? kCostHalf2 : kCostHalf1, kCostQuarter2, &f);
+    }
   }
 
-  __device__ int total() const { return tiles - split + split * f; }
+  // Stream-K runs only in the dense two-consumer kernel with the static schedule.
+  static constexpr bool kStreamK = !GROUPED && MC == 1 && NC == 2 && !SW && !DYN;
+
+  __device__ int total() const {
+    if (kStreamK && p.sk_tiles > 0) return sk_units + tiles - p.sk_tiles;
+    return tiles - split + split * f;
+  }
+
+  // Unit u < sk_units: segment u / workers of pair u % workers's k-block range
+  // (empty units have width 0).  The ranges split the sk_tiles * K-blocks
+  // iterations of the last sk_tiles tiles evenly, in (tile, k-block) order.
+  __device__ Tile at_streamk(int u) const {
+    Tile tl;
+    const int w = u % workers, j = u / workers;
+    const int kb = p.num_k_blocks;
+    const long long lo_i = streamk_begin(w, sk_iters, workers);
+    const long long hi_i = streamk_begin(w + 1, sk_iters, workers);
+    long long pos = lo_i;
+    for (int jj = 0; jj < j && pos < hi_i; ++jj) {
+      const long long end = (pos / kb + 1) * kb;
+      pos = end < hi_i ? end : hi_i;
+    }
+    tl.swap_rows = 0;
+    tl.g = 0;
+    tl.row_end = p.M;
+    if (pos >= hi_i) {
+      tl.width = 0;
+      tl.m0 = tl.n0 = tl.kb0 = tl.kb1 = 0;
+      tl.sk = -1;
+      tl.cmask = 0;
+      return tl;
+    }
+    const long long ts = pos / kb;
+    const long long end = (ts + 1) * kb < hi_i ? (ts + 1) * kb : hi_i;
+    tl.sk = static_cast<int>(ts);
+    tl.kb0 = static_cast<int>(pos - ts * kb);
+    tl.kb1 = static_cast<int>(end - ts * kb);
+    int mt, nt;
+    raster_tile(tiles - p.sk_tiles + tl.sk, rows_of_units, p.num_n_tiles, p.group_m, &mt, &nt);
+    tl.m0 = mt * kTileM;
+    tl.n0 = nt * kTileN;
+    tl.width = kTileN;
+    tl.cmask = (tl.m0 + kRowsPerCta * CG < tl.row_end) ? 3 : 1;
+    return tl;
+  }
 
   __device__ Tile at(int u) const {
+    if constexpr (kStreamK) {
+      if (p.sk_tiles > 0) {
+        if (u < sk_units) return at_streamk(u);
+        u -= sk_units;  // data-parallel tiles: raster order, all but the last sk_tiles
+      }
+    }
     Tile tl;
+    tl.kb0 = 0;
+    tl.kb1 = p.num_k_blocks;
+    tl.sk = -1;
     int t, part, parts;
     unit_part(u, tiles, split, f, &t, &part, &parts);
     int col_off = parts == 1 ? 0 : (part & 1) * (kOutCols / 2);
@@ -287,8 +354,8 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
   const int stride = static_cast<int>((CG == 2) ? num_clusters_x() : gridDim.x);
   // the last-wave cut counts the pairs that run at once: the grid with the
   // static schedule, the co-resident pairs with the dynamic one
-  const Sched<CG, MC, GROUPED, NC, SW> sched(p, t_prefix, t_lo, t_hi, DYN ? p.workers : stride,
-                                             static_cast<int>(pair));
+  const Sched<CG, MC, GROUPED, NC, SW, DYN> sched(p, t_prefix, t_lo, t_hi,
+                                                  DYN ? p.workers : stride, static_cast<int>(pair));
   const int total = sched.total();
   bool aborted = false;
 
@@ -326,6 +393,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
       int s = 0;
       uint32_t ph = 0;
       uint32_t k = 0;  // CLC responses read so far
+      int n_traced = 0;
       if constexpr (DYN) {
         for (uint32_t c = 0; c < kClcSlots; ++c) mbar_arrive_expect_tx(clc_full(c), 16);
       }
@@ -347,6 +415,12 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         if (t >= total) continue;  // a unit past the end (grid rounding): nothing to load
         const Tile tl = sched.at(t);
         if (tl.width == 0) continue;
+        if (p.trace != nullptr && n_traced < kTraceUnits) {
+          unsigned long long* r = p.trace + (static_cast<size_t>(blockIdx.x) * kTraceUnits + n_traced) * 3;
+          r[0] = static_cast<unsigned long long>(t);
+          r[1] = globaltimer_ns();
+          ++n_traced;
+        }
         const uint32_t b_cols = static_cast<uint32_t>(tl.width) / CG;  // this CTA's B columns
         const uint32_t b_chunks = b_cols / 64;
         // Swapped tile: A's rows are the MMA's N, split between the pair; each
@@ -364,7 +438,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         const int b_col = SW ? tl.n0 + static_cast<int>(rank) * p.swiglu_up
                              : tl.n0 + static_cast<int>(rank * b_cols);
         const CUtensorMap* mb = b_map<CG, GROUPED>(P, tl.g);
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, p.timeout_ns)) {
             record_fault(p.err, kFaultTimeout, kRoleProducer, kBarEmpty, s, ph ^ 1u);
             aborted = true;
@@ -431,7 +505,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
           // No rows for this consumer: still commit once per stage (the
           // stage-empty barrier counts every consumer), after the stage's
           // full phase so the commit lands in the right phase.
-          for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
             if (!mbar_wait(full_bar(s), ph, p.timeout_ns)) {
               record_fault(p.err, kFaultTimeout, kRoleMma, kBarFull, s, ph);
               aborted = true;
@@ -462,7 +536,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         const uint32_t idesc =
             swapped ? idesc_with_n(p.idesc_swap, static_cast<uint32_t>((tl.swap_rows + 15) & ~15))
                     : idesc_with_n(p.idesc, static_cast<uint32_t>(tl.width));
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
           if (!mbar_wait(full_bar(s), ph, p.timeout_ns)) {
             record_fault(p.err, kFaultTimeout, kRoleMma, kBarFull, s, ph);
             aborted = true;
@@ -479,7 +553,8 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
             // 128-byte row.  MN-major B: they are 16 rows (2048 bytes) further.
             const uint64_t ad = a_desc + ((kk * 32u) >> 4);
             const uint64_t bd = b_desc + ((kk * 2048u) >> 4);
-            mma_f16<CG>(d_tmem, swapped ? bd : ad, swapped ? ad : bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            mma_f16<CG>(d_tmem, swapped ? bd : ad, swapped ? ad : bd, idesc,
+                        (kb != tl.kb0 || kk != 0) ? 1u : 0u);
           }
           if constexpr (CG == 2)
             mma_commit_pair_mc(empty_bar(s), empty_mask);
@@ -519,11 +594,13 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
     uint32_t acc_ph = 0;
     uint32_t buf = 0;
     uint32_t k = 0;
+    int n_traced = 0;
     for (int t = first; DYN ? t >= 0 : t < total;
          t = next_unit(t, k, kRoleEpilogue, /*arm=*/false, /*warp_wide=*/true)) {
       if (t >= total) continue;
       const Tile tl = sched.at(t);
       if (tl.width == 0 || !((tl.cmask >> cons) & 1)) continue;
+      const int trace_i = n_traced++;  // same unit order as the producer's records
       if (!warp_wait(acc_full_bar(acc), acc_ph, p.timeout_ns)) {
         if (lane == 0) record_fault(p.err, kFaultTimeout, kRoleEpilogue, kBarAccFull, acc, acc_ph);
         aborted = true;
@@ -585,10 +662,96 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
       };
-      for (int sub = 0; sub < nsub; ++sub) {
+      // Stream-K segment of a tile shared by several pairs: every sharer
+      // writes its partial accumulator slice (this warp's 32 rows x 256 FP32
+      // columns) to its slot in the workspace and counts itself in; the last
+      // to arrive sums all slots in slot (= pair) order, so the result does
+      // not depend on which pair finished last, and stores the tile slice.
+      // A slice is laid out [32-column chunk][float4 index][lane] so that each
+      // warp-wide 16-byte store or load covers 512 contiguous bytes.
+      bool store_slice = true;   // false: a partial that another warp will finish
+      const float* fix = nullptr;  // last arriver: this lane's row in slot 0
+      int fix_slots = 0;
+      if constexpr (decltype(sched)::kStreamK) {
+        if (tl.sk >= 0) {
+          int first_w = 0, sharers = 1;
+          streamk_tile_workers(tl.sk, p.num_k_blocks, sched.sk_iters, sched.workers, &first_w,
+                               &sharers);
+          if (sharers > 1) {
+            const uint32_t slice = (static_cast<uint32_t>(cons) * 2u + rank) * 4u + q;
+            constexpr size_t kSliceFloats = 32u * kTileN;
+            const size_t slot_stride = 16u * kSliceFloats;
+            const float* tile_ws = p.ws + static_cast<size_t>(tl.sk) * p.ws_slots * slot_stride +
+                                   slice * kSliceFloats + lane * 4u;
+            float* mine = const_cast<float*>(tile_ws) + (first - first_w) * slot_stride;
+#pragma unroll 1
+            for (int c = 0; c < kTileN / 32; ++c) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(t_acc + c * 32, v);
+              tmem_wait_ld();
+              if (c == kTileN / 32 - 1) release_acc();
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                __stcg(reinterpret_cast<float4*>(mine + (c * 8 + j) * 128),
+                       make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
+            }
+            __threadfence();
+            __syncwarp();
+            int is_last = 0;
+            if (lane == 0) {
+              int* cnt = p.ws_counters + tl.sk * 16 + static_cast<int>(slice);
+              is_last = atomicAdd(cnt, 1) == sharers - 1 ? 1 : 0;
+              if (is_last) *cnt = 0;  // all sharers are in: ready for the next call
+            }
+            is_last = __shfl_sync(0xffffffffu, is_last, 0);
+            if (is_last) {
+              __threadfence();
+              fix = tile_ws;
+              fix_slots = sharers;
+            } else {
+              store_slice = false;
+            }
+          }
+        }
+      }
+      for (int sub = 0; store_slice && sub < nsub; ++sub) {
         uint32_t pk[32];
         const bool last = sub == nsub - 1;
-        if constexpr (SW) {
+        if (fix != nullptr) {
+          // sum of the partial slices, slot by slot, 32 columns at a time
+          const size_t slot_stride = 16u * 32u * kTileN;
+#pragma unroll 1
+          for (int h = 0; h < (out32 ? 1 : 2); ++h) {
+            float acc_v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc_v[j] = 0.f;
+            const int chunk = out32 ? sub : 2 * sub + h;  // 32-column chunk of the slice
+#pragma unroll 1
+            for (int sl = 0; sl < fix_slots; ++sl) {
+              const float* src = fix + sl * slot_stride + chunk * 8 * 128;
+              float4 x[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) x[j] = __ldcg(reinterpret_cast<const float4*>(src + j * 128));
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                acc_v[4 * j] += x[j].x;
+                acc_v[4 * j + 1] += x[j].y;
+                acc_v[4 * j + 2] += x[j].z;
+                acc_v[4 * j + 3] += x[j].w;
+              }
+            }
+            if (out32) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) pk[j] = __float_as_uint(acc_v[j]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                pk[16 * h + i] = outbf ? pack_bf16x2(acc_v[2 * i], acc_v[2 * i + 1])
+                                       : pack_f16x2(acc_v[2 * i], acc_v[2 * i + 1]);
+            }
+          }
+        } else if constexpr (SW) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t g[32], u[32];
@@ -668,6 +831,8 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
           }
         }
       }
+      if (p.trace != nullptr && warp == kEpiWarp0 && lane == 0 && trace_i < kTraceUnits)
+        p.trace[(static_cast<size_t>(blockIdx.x) * kTraceUnits + trace_i) * 3 + 2] = globaltimer_ns();
       if constexpr (NC == 1) {
         if (++acc == 2) {
           acc = 0;

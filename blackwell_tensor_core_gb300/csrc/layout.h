@@ -106,6 +106,31 @@ constexpr int kCostHalf1 = 750;
 constexpr int kCostHalf2 = 833;
 constexpr int kCostQuarter2 = 500;
 
+// Stream-K last wave (two-consumer pair kernel): with T tiles of kb k-blocks
+// on C pairs, the R = T mod C tiles of the last wave (all T when T < C) can
+// be shared out by k-block over all C pairs instead of leaving C - R pairs
+// idle ("B200 的 2CTA 怎样调优": a short last wave idles SMs; split-K-like
+// sharing pays when K is long).  Each pair then does ceil(R*kb/C) iterations
+// of the last wave, plus a fixed cost for writing and summing partial
+// accumulators.  Taken when that beats `cut_cost` (thousandths of a tile-time:
+// 1000 for an uncut last wave, or the cost of the tail_split cut); returns
+// the stream-K tile count (0: not taken) and the most segments one pair's
+// k-block range can touch in *segs.
+constexpr int kStreamKOverhead = 100;
+BWG_HD int streamk_tiles(int T, int C, int kb, int cut_cost, int* segs) {
+  *segs = 0;
+  if (C <= 0 || T <= 0 || kb < 4) return 0;
+  const int R = T % C;
+  // every pair needs a non-empty range: a pair counted among a tile's
+  // sharers must deliver its partial
+  if (R == 0 || static_cast<long long>(R) * kb < C) return 0;
+  const long long per = (static_cast<long long>(R) * kb + C - 1) / C;
+  const long long cost = per * 1000 / kb + kStreamKOverhead;
+  if (cost >= cut_cost) return 0;
+  *segs = static_cast<int>((per + kb - 1) / kb) + 1;
+  return R;
+}
+
 // Two-way form (halves only) for the one-consumer kernels.
 BWG_HD int tail_split_count(int T, int C) {
   int f = 1;

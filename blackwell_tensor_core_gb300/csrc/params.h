@@ -54,7 +54,21 @@ struct GemmParams {
   uint32_t idesc_swap;       // grouped: descriptor of the swapped MMA (A MN-major, B K-major)
   int swiglu_up;             // SwiGLU kernels: first column of the up block in B (= N of H)
   int workers;               // dynamic scheduling: CTA pairs that run at once (last-wave cut)
+  // Stream-K last wave (dense two-consumer kernel, static schedule): the last
+  // sk_tiles tiles of the raster order are shared out by k-blocks over all
+  // pairs; each pair first works through its k-block range (at most sk_segs
+  // segments), then its whole tiles.
+  int sk_tiles;              // 0: no stream-K
+  int sk_segs;
+  int ws_slots;              // partial slots per stream-K tile (most pairs sharing one)
+  float* ws;                 // partials [sk_tiles][ws_slots][16 warp slices][32 rows][256] FP32
+  int* ws_counters;          // arrivals [sk_tiles][16 warp slices], zero between calls
+  // Optional unit trace (nullptr: off): per CTA, kTraceUnits records of
+  // {unit, producer start ns, epilogue end ns} (global timer).
+  unsigned long long* trace;
 };
+
+constexpr int kTraceUnits = 64;
 
 struct GroupedParams {
   GemmParams base;

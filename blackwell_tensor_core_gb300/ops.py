@@ -44,7 +44,8 @@ class PlanInfo(ctypes.Structure):
                 ("coverage", ctypes.c_double), ("smem_input_per_cta", ctypes.c_int),
                 ("smem_total", ctypes.c_int), ("grid", ctypes.c_int), ("tx_bytes", ctypes.c_uint32),
                 ("idesc", ctypes.c_uint32), ("units", ctypes.c_int), ("streamk", ctypes.c_int),
-                ("workers", ctypes.c_int), ("dynamic", ctypes.c_int)]
+                ("workers", ctypes.c_int), ("dynamic", ctypes.c_int), ("sk_tiles", ctypes.c_int),
+                ("sk_segs", ctypes.c_int)]
 
 
 def lib() -> ctypes.CDLL:
@@ -78,6 +79,8 @@ def lib() -> ctypes.CDLL:
                 f = getattr(L, name)
                 f.argtypes = args
                 f.restype = i
+            L.bwg_debug_set_trace.argtypes = [vp]
+            L.bwg_debug_set_trace.restype = None
             L.bwg_set_watchdog_ns.argtypes = [ctypes.c_ulonglong]
             L.bwg_set_watchdog_ns.restype = None
             L.bwg_debug_set_tx_extra.argtypes = [ctypes.c_uint]
@@ -111,6 +114,8 @@ def lib() -> ctypes.CDLL:
             L.bwg_grouped_swap_rows.restype = i
             L.bwg_tail_split_f.argtypes = [i, i, i, ip]
             L.bwg_tail_split_f.restype = i
+            L.bwg_streamk_tiles.argtypes = [i, i, i, i, ip]
+            L.bwg_streamk_tiles.restype = i
             L.bwg_unit_part.argtypes = [i, i, i, i, ip, ip, ip]
             L.bwg_unit_part.restype = None
             L.bwg_version.argtypes = []
@@ -253,6 +258,12 @@ def last_device_error(stream=None) -> tuple[int, int]:
 
 def set_watchdog_ns(ns: int) -> None:
     lib().bwg_set_watchdog_ns(int(ns))
+
+
+def debug_set_trace(buffer: "torch.Tensor | None") -> None:
+    """Profiling hook: per-CTA unit timestamps into `buffer` (int64 CUDA
+    tensor of at least grid * 64 * 3 entries), or None to switch off."""
+    lib().bwg_debug_set_trace(None if buffer is None else buffer.data_ptr())
 
 
 def debug_set_tx_extra(nbytes: int) -> None:

@@ -219,6 +219,17 @@ bwg_status bwg_probe_mma(const void* A, const void* B, float* D, int k_steps, in
  */
 void bwg_debug_set_tx_extra(unsigned int bytes);
 
+/*
+ * Profiling hook: while `buffer` (device memory, or NULL to switch off) is
+ * set, every launch of the dense and grouped pair kernels records, for each
+ * CTA b and each of its first 64 work units i, three 64-bit words at
+ * buffer[(b * 64 + i) * 3]: the unit's index in the schedule, the global
+ * time (ns) when the TMA producer started it, and the global time when the
+ * first epilogue warp finished it.  The buffer needs grid x 64 x 24 bytes;
+ * the caller owns it and reads it after synchronising.
+ */
+void bwg_debug_set_trace(void* buffer);
+
 /* ---------------------------------------------------------------------
  * Host-only planning and layout helpers (no GPU needed; used by tests).
  * ------------------------------------------------------------------- */
@@ -250,12 +261,17 @@ typedef struct {
   int units;               /* work units: tiles, plus one more for every last-wave tile
                               split in two along N (see bwg_tail_split) */
   int streamk;             /* SMALL_M: 1 if (tile, k-block) iterations are shared evenly
-                              over all CTAs (partial tiles summed through a workspace) */
+                              over all CTAs; 2CTA_2C: 1 if the last wave is (see
+                              sk_tiles); partial tiles are summed through a workspace
+                              that the library allocates per stream */
   int workers;             /* CTA pairs (one-CTA kernel: CTAs) that run at once; the
                               last-wave cut is computed for this many */
   int dynamic;             /* 2CTA_2C: 1 if units are claimed at run time by cluster
                               launch control (grid = 2 x units), 0 for the static
                               persistent schedule (grid = 2 x workers) */
+  int sk_tiles;            /* 2CTA_2C: tiles of the last wave shared out by k-block over
+                              all pairs (stream-K; streamk = 1), 0 if none */
+  int sk_segs;             /* 2CTA_2C stream-K: most segments in one pair's range */
 } bwg_plan_info;
 
 /*
@@ -308,6 +324,11 @@ int bwg_tail_split(int T, int C);
  * two-consumer tile 0.833 or 0.5 (their shared-memory bytes per stage);
  * returns the number of cut tiles R (0: none) and stores f. */
 int bwg_tail_split_f(int T, int C, int max_f, int* f);
+/* Stream-K last wave of the two-consumer kernel (see streamk_tiles in the
+   library's scheduler): tiles shared out by k-block, 0 if the last wave
+   (costing cut_cost thousandths of a tile-time) is kept; *segs = most
+   segments in one pair's k-block range. */
+int bwg_streamk_tiles(int T, int C, int kb, int cut_cost, int* segs);
 
 /* Unit u of a schedule whose last R tiles are cut into f parts: tile index,
  * part (0 .. f-1) and parts of that tile (1 or f). */

@@ -470,3 +470,48 @@ def test_host_entry_point_8192_sampled():
     hD, _ = _host_call(c.A, c.B, c.out_dtype)
     torch.cuda.current_stream().synchronize()
     _check_sampled(c.A, c.B, hD, 8000, 17, c.name + " host entry")
+
+
+# --------------------------------------------- stream-K last wave (dense) ---
+
+@pytest.mark.parametrize("shape", [(2560, 4864, 512), (2560, 4864, 520), (1024, 1024, 4096),
+                                   (600, 2048, 1024)])
+def test_streamk_last_wave_exact_and_repeatable(shape, monkeypatch):
+    """Two-consumer kernel with the last wave shared out by k-block: 95 tiles
+    (19 stream-K tiles, 4 pairs each), a ragged last k-block, 8 tiles over 76
+    pairs (about 10 sharers a tile), ragged M.  Exact on integer inputs,
+    FP32 and BF16 output, and bit-identical run to run on random inputs
+    (partials are summed in pair order)."""
+    from blackwell_tensor_core_gb300 import ops
+    monkeypatch.setenv("BWG_STREAMK_DENSE", "1")
+    M, N, K = shape
+    pl = ops.plan(M, N, K, wl.OUT_FP32, force_kernel=ops.KERNEL_2CTA_2C)
+    assert pl.streamk == 1 and pl.sk_tiles > 0
+    g = wl.generator(5900 + K)
+    A = wl.randint_matrix(M, K, -2, 2, g)
+    B = wl.randint_matrix(K, N, -2, 2, g)
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+    D, _ = gpu_gemm(A, B, wl.OUT_FP32, "2cta_2c")
+    assert np.array_equal(D.double().numpy(), Dref)
+    D16, _ = gpu_gemm(A, B, wl.OUT_BF16, "2cta_2c")
+    assert_bits_equal(D16, oracle.round_to(Dref, "bf16"), "stream-K bf16 %s" % (shape,))
+    Ar = wl.normal_matrix(M, K, 1.0, g)
+    Br = wl.normal_matrix(K, N, 1.0, g)
+    R1, _ = gpu_gemm(Ar, Br, wl.OUT_FP32, "2cta_2c")
+    R2, _ = gpu_gemm(Ar, Br, wl.OUT_FP32, "2cta_2c")
+    assert torch.equal(R1, R2)
+    Rref, S = oracle.gemm(wl.bits(Ar), wl.bits(Br))
+    assert_within_bound(R1, Rref, S, "stream-K random %s" % (shape,))
+
+
+def test_streamk_off_matches_on_at_4096(monkeypatch):
+    """4096^3 (52 of 128 tiles shared out): stream-K and the plain last wave
+    give results within the bound on sampled outputs."""
+    from blackwell_tensor_core_gb300 import ops
+    c = wl.square_case()
+    D0, _ = gpu_gemm(c.A, c.B, c.out_dtype)
+    monkeypatch.setenv("BWG_STREAMK_DENSE", "1")
+    assert ops.plan(4096, 4096, 4096).streamk == 1
+    D1, _ = gpu_gemm(c.A, c.B, c.out_dtype)
+    _check_sampled(c.A, c.B, D1, 4000, 31, "4096 stream-K")
+    _check_sampled(c.A, c.B, D0, 4000, 31, "4096 plain")

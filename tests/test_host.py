@@ -70,6 +70,35 @@ def test_dynamic_schedule_plan(ops, monkeypatch):
     assert ops.plan(8192, 8192, 8192, force_kernel=ops.KERNEL_2CTA).dynamic == 0
 
 
+def test_streamk_last_wave_plan(ops, monkeypatch):
+    """Stream-K of the last wave (opt-in): taken for 4096^3 (52 of 128 tiles)
+    and 8192^3 (56 of 512), not when the tiles fill whole waves, not for K
+    below 4 k-blocks; the per-pair segment bound covers every pair's range."""
+    assert ops.plan(4096, 4096, 4096).streamk == 0  # off by default
+    monkeypatch.setenv("BWG_STREAMK_DENSE", "1")
+    p = ops.plan(4096, 4096, 4096)
+    assert (p.kernel, p.streamk, p.sk_tiles, p.workers) == (ops.KERNEL_2CTA_2C, 1, 52, 76)
+    assert p.units == p.sk_segs * 76 + 128 - 52
+    assert ops.plan(8192, 8192, 8192).sk_tiles == 56
+    assert ops.plan(4096, 4096, 64).streamk == 0
+    assert ops.plan(512 * 76 // 4, 1024, 4096).sk_tiles == 0  # 76 tiles: whole waves
+    monkeypatch.setenv("BWG_STREAMK_DENSE", "0")
+    assert ops.plan(4096, 4096, 4096).streamk == 0
+    L = ops.lib()
+    for T, C, kb in [(128, 76, 64), (512, 76, 128), (95, 76, 8), (8, 76, 64), (10, 3, 7)]:
+        segs = ctypes.c_int(0)
+        R = L.bwg_streamk_tiles(T, C, kb, 1 << 30, ctypes.byref(segs))
+        assert R == T % C
+        W = R * kb
+        for w in range(C):
+            lo, hi = W * w // C, W * (w + 1) // C
+            pos, n = lo, 0
+            while pos < hi:
+                pos = min((pos // kb + 1) * kb, hi)
+                n += 1
+            assert n <= segs.value, (T, C, kb, w)
+
+
 def test_status_strings(ops):
     assert ops.status_string(0) == "ok"
     assert "align" in ops.status_string(2)
@@ -279,7 +308,7 @@ def test_plan_reports_split_units(ops):
     assert mid.units == 256 + 256 % 76
     two = ops.plan(8192, 8192, 8192)
     # remainder 56 of 76: quarters (3 x 0.5) and halves (2 x 0.833) both lose to 1.0
-    assert two.tiles == 512 and two.units == 512
+    assert two.tiles == 512 and two.sk_tiles == 0 and two.units == 512
     assert ops.plan(2048, 5120, 128).units == 80 - 4 + 4 * 4       # 4 left over: quarters
     assert ops.plan(1024, 13568, 64).units == 106 - 30 + 2 * 30    # 30 left over: halves
 
