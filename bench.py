@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -107,6 +108,16 @@ class ClockSampler:
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
+            return
+        # nvidia-smi's first query initialises NVML, which can hold up CUDA
+        # launches from this process for seconds: wait for its first sample
+        # so that the set-up does not fall inside the timed region.
+        t0 = time.monotonic()
+        while time.monotonic() - t0 < 20.0 and self.proc.poll() is None:
+            self.out.flush()
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.05)
 
     def stop(self):
         if self.proc is None:
@@ -140,11 +151,23 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
-def kernel_source_hash() -> str:
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source with comments and blank space removed, so that the
+    hash below changes with the code, not with its comments."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_source_hash(read=None) -> str:
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "blackwell_tensor_core_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        if read is None:
+            with open(os.path.join(ROOT, "blackwell_tensor_core_gb300", "csrc", name), encoding="utf-8") as f:
+                text = f.read()
+        else:
+            text = read(name)
+        h.update(_code_only(text).encode())
     return h.hexdigest()[:16]
 
 
@@ -429,7 +452,8 @@ def run_ours(args, rank, world, local):
 
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
-    time.sleep(0.3)
+    for _ in range(3):  # keep the clocks up after the sampler's start-up
+        launch()
     total_ms, per = time_launches(launch, args.steps, stream, dist_mod)
     clocks = sampler.stop()
     check_device_error(ops)

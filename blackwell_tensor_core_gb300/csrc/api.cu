@@ -737,10 +737,11 @@ bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
 
 // ------------------------------------------- no-allocation small-M path -----
 //
-// Some callers cannot let a library call cudaMalloc: code that runs while a
-// stream is being captured into a CUDA graph (allocation calls are not
-// allowed there), processes that hand all device memory to their own pool
-// allocator, and real-time loops that must not block on the allocator.  For
+// Some callers cannot let a library call cudaMalloc: processes that hand all
+// device memory to their own pool allocator up front (an allocation from the
+// library would fail or eat into that budget), and real-time loops that must
+// not block on the allocator (cudaMalloc can stall the host and synchronise
+// the device).  For
 // them gemm_bf16_small_m_noalloc runs the stream-K small-M kernel with its
 // partial sums and tile counters in the fixed device array below instead of
 // the per-stream workspace that gemm_bf16 allocates.

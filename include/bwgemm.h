@@ -121,10 +121,11 @@ bwg_status grouped_gemm_swiglu_fp16(const void* A, const void* const* B, void* H
 /*
  * No-allocation form of gemm_bf16 for small M (M <= 128).  The pages have no
  * counterpart: it exists for callers that cannot let the library call
- * cudaMalloc -- code running while a stream is captured into a CUDA graph
- * (allocation is not allowed there), programs that give all device memory to
- * their own pool allocator, and latency-critical loops that must not wait on
- * the allocator.  It computes what gemm_bf16 computes (same arguments and
+ * cudaMalloc -- programs that hand all device memory to their own pool
+ * allocator up front (a cudaMalloc from the library would then fail or eat
+ * into that budget), and latency-critical loops that must not wait on the
+ * allocator (cudaMalloc can block the host and synchronise the device).
+ * It computes what gemm_bf16 computes (same arguments and
  * rules) with the stream-K small-M kernel, keeping that kernel's partial sums
  * and per-tile counters in one fixed 32 MiB device array inside the library
  * instead of an allocated workspace:

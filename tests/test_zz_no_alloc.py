@@ -1,8 +1,8 @@
 """The no-allocation small-M entry point, checked against gemm_bf16.
 
 gemm_bf16_small_m_noalloc is for callers that cannot let the library call
-cudaMalloc (for example while a stream is captured into a CUDA graph, or when
-all device memory belongs to the caller's own pool): it keeps the stream-K
+cudaMalloc (all device memory handed to the caller's own pool allocator, or a
+loop that must never stall on the allocator): it keeps the stream-K
 kernel's partial sums in a fixed device array of the library.  This file runs
 last so that, should it fail, every other test has already run; it also
 passes on its own in a fresh process.  Each case makes two calls in a row on
