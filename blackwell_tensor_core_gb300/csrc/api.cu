@@ -575,6 +575,7 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
     p.idesc = pl.idesc;
     p.tx_extra = g_tx_extra.load();
     p.streamk = pl.streamk;
+    p.trace = g_trace.load();
     if (pl.streamk) {
       p.ws_slots = streamk_max_sharers(pl.tiles, pl.k_blocks, pl.grid);
       Workspace w;

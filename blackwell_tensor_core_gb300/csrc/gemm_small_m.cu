@@ -98,6 +98,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31u;
   const int S = p.stages;
+  unsigned long long* const trace = p.trace != nullptr ? p.trace + 8u * blockIdx.x : nullptr;
+  if (trace != nullptr && threadIdx.x == 0) trace[0] = globaltimer_ns();
   const uint32_t at_stage_bytes = static_cast<uint32_t>(p.m_pad) * kBK * 2;  // m_pad rows x 128 B
   const uint32_t stage_bytes = kBtStageBytes + at_stage_bytes;
   const int out_elt = p.out_dtype == kOutF32 ? 4 : 2;
@@ -124,13 +126,63 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
       mbar_init(acc_empty_bar(a), 4);
     }
     fence_mbarrier_init();
-  }
-  if (warp == 0 && lane == 0) {
     prefetch_tensormap(&p.map_bt);
     prefetch_tensormap(&p.map_at);
     prefetch_tensormap(&p.map_d);
     if (p.tile_n > 64) prefetch_tensormap(&p.map_d2);
   }
+  const Segments segs(p);
+  bool aborted = false;
+  // TMA producer (warp 0, lane 0): walks this CTA's segments k-block by
+  // k-block.  It is the thread that initialised the barriers, so it fills
+  // the first ring stages before the block-wide barrier below: the first
+  // loads are in flight while TMEM is being allocated.
+  struct Producer {
+    const SmallMParams& p;
+    const Segments& segs;
+    uint32_t smem_bt, smem_at, at_stage_bytes, bar0, tx;
+    int S, i = 0, kb = 0, kb1 = 0, n0 = 0, s = 0;
+    uint32_t ph = 0;
+    bool have = false, done = false;
+    __device__ void issue(int limit, bool* aborted) {
+      for (int n = 0; n < limit && !done && !*aborted;) {
+        if (!have) {
+          int t, kb0;
+          if (!segs.get(i, &t, &kb0, &kb1)) {
+            done = true;
+            break;
+          }
+          n0 = t * p.tile_n;
+          kb = kb0;
+          have = true;
+        }
+        if (kb >= kb1) {
+          have = false;
+          ++i;
+          continue;
+        }
+        const uint32_t full = bar0 + 8u * s, empty = bar0 + 8u * (S + s);
+        if (!mbar_wait(empty, ph ^ 1u, p.timeout_ns)) {
+          record_fault_small(p.err, 0, 1, s, ph ^ 1u);
+          *aborted = true;
+          break;
+        }
+        const int k0 = kb * kBK;
+        const uint32_t sbt = smem_bt + s * kBtStageBytes;
+        mbar_arrive_expect_tx(full, tx);
+        tma_load_2d(sbt, &p.map_bt, full, n0, k0);
+        tma_load_2d(sbt + kBtChunkBytes, &p.map_bt, full, n0 + 64, k0);
+        tma_load_2d(smem_at + s * at_stage_bytes, &p.map_at, full, k0, 0);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+        ++kb;
+        ++n;
+      }
+    }
+  } producer{p, segs, smem_bt, smem_at, at_stage_bytes, smem_bar, stage_bytes + p.tx_extra, S};
+  if (threadIdx.x == 0) producer.issue(S, &aborted);
   if (warp == 1) {
     tmem_alloc<1>(tmem_slot, kTmemCols);
     tmem_relinquish<1>();
@@ -139,36 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = ld_shared_u32(tmem_slot);
-  const Segments segs(p);
-  bool aborted = false;
 
   if (warp == 0) {
-    if (lane == 0) {
-      int s = 0;
-      uint32_t ph = 0;
-      const uint32_t tx = stage_bytes + p.tx_extra;
-      int t, kb0, kb1;
-      for (int i = 0; !aborted && segs.get(i, &t, &kb0, &kb1); ++i) {
-        const int n0 = t * p.tile_n;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(empty_bar(s), ph ^ 1u, p.timeout_ns)) {
-            record_fault_small(p.err, 0, 1, s, ph ^ 1u);
-            aborted = true;
-            break;
-          }
-          const int k0 = kb * kBK;
-          const uint32_t sbt = smem_bt + s * kBtStageBytes;
-          mbar_arrive_expect_tx(full_bar(s), tx);
-          tma_load_2d(sbt, &p.map_bt, full_bar(s), n0, k0);
-          tma_load_2d(sbt + kBtChunkBytes, &p.map_bt, full_bar(s), n0 + 64, k0);
-          tma_load_2d(smem_at + s * at_stage_bytes, &p.map_at, full_bar(s), k0, 0);
-          if (++s == S) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-      }
-    }
+    if (lane == 0) producer.issue(0x7FFFFFFF, &aborted);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
@@ -191,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
             aborted = true;
             break;
           }
+          if (trace != nullptr && i == 0 && kb == kb0) trace[1] = globaltimer_ns();
           tc_fence_after();
           // MMA A = B^T tile (MN-major, two 64-channel boxes 8 KiB apart),
           // MMA B = A tile (K-major, 128-byte rows, 8-row groups 1 KiB apart).
@@ -209,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
         }
         if (aborted) break;
         mma_commit_1cta(acc_full_bar(acc));
+        if (trace != nullptr) trace[2] = globaltimer_ns();
         if (++acc == 2) {
           acc = 0;
           acc_ph ^= 1u;
@@ -233,18 +260,30 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
     uint32_t acc_ph = 0;
     int t, kb0, kb1;
 
-    // One value of D (row r, this thread's column) into the staging tile.
-    // Staging half h is a dense [m_pad][pitch_h] tile, pitch_0 = min(64, tile_n),
-    // pitch_1 = tile_n - 64: exactly the box of the TMA store that writes it.
-    auto stage_value = [&](int r, float x) {
+    // Rows r0 .. r0+15 of this thread's column (those below M) into the
+    // staging tile.  Staging half h is a dense [m_pad][pitch_h] tile, pitch_0 =
+    // min(64, tile_n), pitch_1 = tile_n - 64: exactly the box of the TMA store
+    // that writes it.  The epilogue runs once per tile with its code fetched
+    // cold, so it is kept short: one conversion and one store per value, in a
+    // body that the row loops below reuse.
+    const uint32_t row_bytes = pitch * static_cast<uint32_t>(out_elt);
+    const uint32_t col_addr = smem_d + half * half_bytes + col_in_half * static_cast<uint32_t>(out_elt);
+    auto stage16 = [&](int r0, const uint32_t (&v)[16]) {
       if (!stores) return;
-      const uint32_t tile = smem_d + half * half_bytes;
+      const int n = min(16, p.M - r0);
+      const uint32_t a = col_addr + static_cast<uint32_t>(r0) * row_bytes;
       if (out32) {
-        st_shared_u32(tile + (static_cast<uint32_t>(r) * pitch + col_in_half) * 4u, __float_as_uint(x));
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+          if (r < n) st_shared_u32(a + r * row_bytes, v[r]);
+      } else if (outbf) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+          if (r < n) st_shared_u16(a + r * row_bytes, cvt_rn_bf16(__uint_as_float(v[r])));
       } else {
-        const uint32_t h = outbf ? pack_bf16x2(x, 0.f) : pack_f16x2(x, 0.f);
-        st_shared_u16(tile + (static_cast<uint32_t>(r) * pitch + col_in_half) * 2u,
-                      static_cast<uint16_t>(h & 0xFFFFu));
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+          if (r < n) st_shared_u16(a + r * row_bytes, cvt_rn_f16(__uint_as_float(v[r])));
       }
     };
     auto store_staged = [&](int n0) {
@@ -269,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
         break;
       }
       tc_fence_after();
+      if (trace != nullptr && store_thread) trace[4] = globaltimer_ns();
       // The previous TMA store must have finished reading the staging tile.
       if (store_thread) bulk_wait_group_read<0>();
       named_bar_sync(1, 128);
@@ -279,28 +319,31 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
         streamk_tile_workers(t, p.num_k_blocks, segs.W, gridDim.x, &first, &sharers);
         slot = p.ws + (static_cast<size_t>(t) * p.ws_slots + (blockIdx.x - first)) * slot_floats;
       }
-      for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(t_acc + c0, v);
+#pragma unroll 1
+      for (int c0 = 0; c0 < p.m_pad; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(t_acc + c0, v);
         tmem_wait_ld();
-        if (c0 + 32 >= p.m_pad) {
+        if (trace != nullptr && store_thread && c0 == 0) trace[5] = globaltimer_ns();
+        if (c0 + 16 >= p.m_pad) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_local(acc_empty_bar(acc));
         }
-        const int rows = min(32, p.M - c0);
         if (whole) {
-#pragma unroll
-          for (int r = 0; r < 32; ++r)
-            if (r < rows) stage_value(c0 + r, __uint_as_float(v[r]));
+          stage16(c0, v);
+          if (trace != nullptr && store_thread && c0 == 0) trace[6] = globaltimer_ns();
         } else {
           // partial accumulator -> workspace slot, [row][128 columns] FP32
+          const int n = min(16, p.M - c0);
+          float* dst = slot + static_cast<size_t>(c0) * 128u + ch;
 #pragma unroll
-          for (int r = 0; r < 32; ++r)
-            if (r < rows) slot[static_cast<size_t>(c0 + r) * 128u + ch] = __uint_as_float(v[r]);
+          for (int r = 0; r < 16; ++r)
+            if (r < n) dst[r * 128] = __uint_as_float(v[r]);
         }
       }
       if (whole) {
+        if (trace != nullptr && store_thread) trace[7] = globaltimer_ns();
         store_staged(n0);
       } else {
         // Publish the partial, count it; the last sharer sums all slots.
@@ -319,23 +362,39 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
           // loads of a thread are independent (and coalesced across the
           // warp), so they are all in flight together.
           const float* tile_slots = p.ws + static_cast<size_t>(t) * p.ws_slots * slot_floats;
+#pragma unroll 1
           for (int c0 = 0; c0 < p.M; c0 += 32) {
             const int rows = min(32, p.M - c0);
-            float sum[32];
+            const float* src = tile_slots + static_cast<size_t>(c0) * 128u + ch;
+            float sum[32], cur[32];
 #pragma unroll
-            for (int r = 0; r < 32; ++r) sum[r] = 0.f;
-            for (int sl = 0; sl < sharers; ++sl) {
-              const float* src = tile_slots + static_cast<size_t>(sl) * slot_floats +
-                                 static_cast<size_t>(c0) * 128u + ch;
-              float v[32];
-#pragma unroll
-              for (int r = 0; r < 32; ++r) v[r] = (r < rows) ? __ldcg(src + r * 128) : 0.f;
-#pragma unroll
-              for (int r = 0; r < 32; ++r) sum[r] += v[r];
+            for (int r = 0; r < 32; ++r) {
+              sum[r] = 0.f;
+              cur[r] = (r < rows) ? __ldcg(src + r * 128) : 0.f;
             }
+            // Two slots in flight: the next slot's loads are issued before
+            // the current one is added.
+#pragma unroll 1
+            for (int sl = 0; sl < sharers; ++sl) {
+              float nxt[32];
+              const float* ns = src + static_cast<size_t>(sl + 1) * slot_floats;
+              const bool more = sl + 1 < sharers;
 #pragma unroll
-            for (int r = 0; r < 32; ++r)
-              if (r < rows) stage_value(c0 + r, sum[r]);
+              for (int r = 0; r < 32; ++r) nxt[r] = (more && r < rows) ? __ldcg(ns + r * 128) : 0.f;
+#pragma unroll
+              for (int r = 0; r < 32; ++r) {
+                sum[r] += cur[r];
+                cur[r] = nxt[r];
+              }
+            }
+            uint32_t lo[16], hi[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+              lo[r] = __float_as_uint(sum[r]);
+              hi[r] = __float_as_uint(sum[16 + r]);
+            }
+            stage16(c0, lo);
+            if (rows > 16) stage16(c0 + 16, hi);
           }
           store_staged(n0);
         }
@@ -345,7 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
         acc_ph ^= 1u;
       }
     }
-    if (store_thread) bulk_wait_group<0>();
+    // The CTA may exit once the TMA stores have read the staging tile; their
+    // global writes complete on their own before the grid is done.
+    if (store_thread) {
+      bulk_wait_group_read<0>();
+      if (trace != nullptr) trace[3] = globaltimer_ns();
+    }
     __syncwarp();
   }
 

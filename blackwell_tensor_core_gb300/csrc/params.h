@@ -91,6 +91,9 @@ struct SmallMParams {
   int ws_slots;      // partial-accumulator slots per tile (most CTAs sharing a tile)
   float* ws;         // stream-K partials: [num_tiles][ws_slots][m_pad][128] FP32
   int* ws_counters;  // stream-K arrival counters, one per tile, zero between calls
+  // Optional trace (nullptr: off): per CTA eight global-timer stamps (ns),
+  // documented with bwg_debug_set_trace.
+  unsigned long long* trace;
 };
 
 // Host launchers (one per kernel instantiation).  They only enqueue.

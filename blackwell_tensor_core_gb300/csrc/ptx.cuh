@@ -374,4 +374,29 @@ BWG_DEV void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
+// Warp-collective TMEM load of 16 consecutive 32-bit columns (see above).
+BWG_DEV void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// One FP32 value rounded to nearest even, as the 16 bits of a BF16 / FP16.
+BWG_DEV uint16_t cvt_rn_bf16(float x) {
+  uint16_t h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(x));
+  return h;
+}
+
+BWG_DEV uint16_t cvt_rn_f16(float x) {
+  uint16_t h;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(x));
+  return h;
+}
+
 }  // namespace bwg

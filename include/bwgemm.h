@@ -227,7 +227,13 @@ void bwg_debug_set_tx_extra(unsigned int bytes);
  * buffer[(b * 64 + i) * 3]: the unit's index in the schedule, the global
  * time (ns) when the TMA producer started it, and the global time when the
  * first epilogue warp finished it.  The buffer needs grid x 64 x 24 bytes;
- * the caller owns it and reads it after synchronising.
+ * the caller owns it and reads it after synchronising.  Launches of the
+ * small-M kernel through gemm_bf16 / gemm_fp16 record instead eight words per
+ * CTA b at buffer[8 * b] (grid x 64 bytes), global times in ns (0: not
+ * reached): [0] kernel entry, [1] first stage seen by the MMA issuer, [2] last
+ * accumulator committed, [3] epilogue finished, [4] accumulator seen by the
+ * epilogue, [5] first TMEM load done, [6] first rows staged, [7] last rows
+ * staged (the last three for whole-tile segments).
  */
 void bwg_debug_set_trace(void* buffer);
 
