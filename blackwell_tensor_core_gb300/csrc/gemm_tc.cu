@@ -416,7 +416,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         const Tile tl = sched.at(t);
         if (tl.width == 0) continue;
         if (p.trace != nullptr && n_traced < kTraceUnits) {
-          unsigned long long* r = p.trace + (static_cast<size_t>(blockIdx.x) * kTraceUnits + n_traced) * 3;
+          unsigned long long* r = p.trace + (static_cast<size_t>(blockIdx.x) * kTraceUnits + n_traced) * kTraceWords;
           r[0] = static_cast<unsigned long long>(t);
           r[1] = globaltimer_ns();
           ++n_traced;
@@ -607,6 +607,10 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         break;
       }
       tc_fence_after();
+      const bool tracer = p.trace != nullptr && warp == kEpiWarp0 && lane == 0 && trace_i < kTraceUnits;
+      unsigned long long* const trec =
+          tracer ? p.trace + (static_cast<size_t>(blockIdx.x) * kTraceUnits + trace_i) * kTraceWords : nullptr;
+      if (tracer) trec[3] = globaltimer_ns();
       const int row_w = tl.m0 + cons * 2 * kRowsPerCta + static_cast<int>(rank * kRowsPerCta + q * 32u);
       const uint32_t t_acc = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc) * kTileN;
       if (GROUPED && tl.swap_rows > 0) {
@@ -661,6 +665,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
+        if (tracer) trec[4] = globaltimer_ns();
       };
       // Stream-K segment of a tile shared by several pairs: every sharer
       // writes its partial accumulator slice (this warp's 32 rows x 256 FP32
@@ -715,7 +720,122 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
           }
         }
       }
-      for (int sub = 0; store_slice && sub < nsub; ++sub) {
+      // Stage one 32-row x sub_cols sub-tile (packed in pk) and store it.
+      auto emit = [&](int sub, const uint32_t (&pk)[32]) __attribute__((always_inline)) {
+        const int col0 = tl.n0 + sub * sub_cols;
+        if (col0 >= p.N) return;
+        const bool whole_box = !p.direct_store && (!GROUPED || (row_w + 32 <= tl.row_end));
+        if (whole_box) {
+          if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
+          __syncwarp();
+          const uint32_t sb = ebuf + buf * kEpiBufBytes;
+#pragma unroll
+          for (uint32_t j = 0; j < 8; ++j)
+            st_shared_v4(sb + swizzle128_offset(lane, j), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                         pk[4 * j + 3]);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.map_d, sb, col0, row_w);
+            bulk_commit_group();
+          }
+          buf = (buf + 1u) % kEpiBufs;
+        } else {
+          // Ragged end of a group, or the register-store epilogue: each
+          // thread stores its own row (64 or 32 columns), if inside.
+          const int row = row_w + static_cast<int>(lane);
+          if (row < tl.row_end) {
+            const int elt = out32 ? 4 : 2;
+            uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) +
+                            (static_cast<size_t>(row) * p.ldd + col0) * elt;
+            const int ncols = min(sub_cols, p.N - col0);
+            if (ncols == sub_cols) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                reinterpret_cast<uint4*>(drow)[j] =
+                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            } else if (out32) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                if (c < ncols) reinterpret_cast<uint32_t*>(drow)[c] = pk[c];
+            } else {
+#pragma unroll
+              for (int c = 0; c < 64; ++c)
+                if (c < ncols)
+                  reinterpret_cast<uint16_t*>(drow)[c] =
+                      static_cast<uint16_t>(pk[c >> 1] >> ((c & 1) * 16));
+            }
+          }
+        }
+      };
+      // Two consumers: both accumulators of a pair fill at the same time, so
+      // the tensor pipe waits until the epilogue hands them back.  For 16-bit
+      // output the warp therefore reads its whole 32 x 256 slice out of TMEM
+      // first (packed to 16 bits: 128 registers), releases the accumulator,
+      // and only then stages and stores it, while the next tile's MMAs run.
+      const bool early = NC == 2 && !out32 && fix == nullptr && store_slice;
+      if constexpr (NC == 2) {
+        if (early) {
+          if constexpr (SW) {
+            uint32_t pks[2][32];
+#pragma unroll
+            for (int sub = 0; sub < 2; ++sub) {
+              if (sub < nsub) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  uint32_t g[32], u[32];
+                  tmem_ld_32x32b_x32(t_acc + sub * 64 + h * 32, g);
+                  tmem_ld_32x32b_x32(t_acc + out_cols + sub * 64 + h * 32, u);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) {
+                    const float y0 = swiglu_f32(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]));
+                    const float y1 =
+                        swiglu_f32(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]));
+                    pks[sub][16 * h + i] = outbf ? pack_bf16x2(y0, y1) : pack_f16x2(y0, y1);
+                  }
+                }
+              }
+            }
+            release_acc();
+#pragma unroll
+            for (int sub = 0; sub < 2; ++sub)
+              if (sub < nsub) emit(sub, pks[sub]);
+          } else {
+            // Sub-tile 0 goes straight to its staging box (the previous
+            // tile's stores finished long ago) and its TMA store starts; the
+            // other three stay in registers (96) until the hand-back.
+            auto load_packed = [&](int sub, uint32_t (&pk)[32]) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(t_acc + sub * 64 + h * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const float lo = __uint_as_float(v[2 * i]), hi = __uint_as_float(v[2 * i + 1]);
+                  pk[16 * h + i] = outbf ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
+                }
+              }
+            };
+            {
+              uint32_t pk0[32];
+              load_packed(0, pk0);
+              if (nsub == 1) release_acc();
+              emit(0, pk0);
+            }
+            uint32_t pka[3][32];
+#pragma unroll
+            for (int sub = 1; sub < 4; ++sub)
+              if (sub < nsub) load_packed(sub, pka[sub - 1]);
+            if (nsub > 1) release_acc();
+#pragma unroll
+            for (int sub = 1; sub < 4; ++sub)
+              if (sub < nsub) emit(sub, pka[sub - 1]);
+          }
+        }
+      }
+      for (int sub = 0; store_slice && !early && sub < nsub; ++sub) {
         uint32_t pk[32];
         const bool last = sub == nsub - 1;
         if (fix != nullptr) {
@@ -785,54 +905,10 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
             pk[16 + i] = outbf ? pack_bf16x2(lo1, hi1) : pack_f16x2(lo1, hi1);
           }
         }
-        const int col0 = tl.n0 + sub * sub_cols;
-        if (col0 >= p.N) continue;
-        const bool whole_box = !p.direct_store && (!GROUPED || (row_w + 32 <= tl.row_end));
-        if (whole_box) {
-          if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
-          __syncwarp();
-          const uint32_t sb = ebuf + buf * kEpiBufBytes;
-#pragma unroll
-          for (uint32_t j = 0; j < 8; ++j)
-            st_shared_v4(sb + swizzle128_offset(lane, j), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
-                         pk[4 * j + 3]);
-          fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&p.map_d, sb, col0, row_w);
-            bulk_commit_group();
-          }
-          buf = (buf + 1u) % kEpiBufs;
-        } else {
-          // Ragged end of a group, or the register-store epilogue: each
-          // thread stores its own row (64 or 32 columns), if inside.
-          const int row = row_w + static_cast<int>(lane);
-          if (row < tl.row_end) {
-            const int elt = out32 ? 4 : 2;
-            uint8_t* drow = static_cast<uint8_t*>(p.d_ptr) +
-                            (static_cast<size_t>(row) * p.ldd + col0) * elt;
-            const int ncols = min(sub_cols, p.N - col0);
-            if (ncols == sub_cols) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                reinterpret_cast<uint4*>(drow)[j] =
-                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-            } else if (out32) {
-#pragma unroll
-              for (int c = 0; c < 32; ++c)
-                if (c < ncols) reinterpret_cast<uint32_t*>(drow)[c] = pk[c];
-            } else {
-#pragma unroll
-              for (int c = 0; c < 64; ++c)
-                if (c < ncols)
-                  reinterpret_cast<uint16_t*>(drow)[c] =
-                      static_cast<uint16_t>(pk[c >> 1] >> ((c & 1) * 16));
-            }
-          }
-        }
+        emit(sub, pk);
       }
       if (p.trace != nullptr && warp == kEpiWarp0 && lane == 0 && trace_i < kTraceUnits)
-        p.trace[(static_cast<size_t>(blockIdx.x) * kTraceUnits + trace_i) * 3 + 2] = globaltimer_ns();
+        p.trace[(static_cast<size_t>(blockIdx.x) * kTraceUnits + trace_i) * kTraceWords + 2] = globaltimer_ns();
       if constexpr (NC == 1) {
         if (++acc == 2) {
           acc = 0;

@@ -64,11 +64,12 @@ struct GemmParams {
   float* ws;                 // partials [sk_tiles][ws_slots][16 warp slices][32 rows][256] FP32
   int* ws_counters;          // arrivals [sk_tiles][16 warp slices], zero between calls
   // Optional unit trace (nullptr: off): per CTA, kTraceUnits records of
-  // {unit, producer start ns, epilogue end ns} (global timer).
+  // kTraceWords words (global timer, ns).
   unsigned long long* trace;
 };
 
 constexpr int kTraceUnits = 64;
+constexpr int kTraceWords = 5;  // unit, producer start, epilogue end, accumulator seen, released
 
 struct GroupedParams {
   GemmParams base;

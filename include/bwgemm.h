@@ -223,10 +223,12 @@ void bwg_debug_set_tx_extra(unsigned int bytes);
 /*
  * Profiling hook: while `buffer` (device memory, or NULL to switch off) is
  * set, every launch of the dense and grouped pair kernels records, for each
- * CTA b and each of its first 64 work units i, three 64-bit words at
- * buffer[(b * 64 + i) * 3]: the unit's index in the schedule, the global
- * time (ns) when the TMA producer started it, and the global time when the
- * first epilogue warp finished it.  The buffer needs grid x 64 x 24 bytes;
+ * CTA b and each of its first 64 work units i, five 64-bit words at
+ * buffer[(b * 64 + i) * 5]: the unit's index in the schedule, the global
+ * time (ns) when the TMA producer started it, the global time when the
+ * first epilogue warp finished it, and when that warp saw the accumulator
+ * full and handed it back to the MMA issuer.  The buffer needs
+ * grid x 64 x 40 bytes;
  * the caller owns it and reads it after synchronising.  Launches of the
  * small-M kernel through gemm_bf16 / gemm_fp16 record instead eight words per
  * CTA b at buffer[8 * b] (grid x 64 bytes), global times in ns (0: not
