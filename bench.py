@@ -190,8 +190,11 @@ def recorded_traffic():
 
 # ------------------------------------------------------------- timing -------
 
-def time_launches(launch, steps, stream, dist_mod, between=None):
-    """Times `steps` launches on `stream`.  Returns (total_ms, per-launch ms list)."""
+def time_launches(launch, steps, stream, dist_mod, between=None, keep_ahead=False):
+    """Times `steps` launches on `stream`.  Returns (total_ms, per-launch ms list).
+    keep_ahead: a GPU sleep before the first timed launch lets the host queue
+    the launches ahead of the GPU, so that short kernels are timed without
+    host gaps (the sleep lies outside every timed interval)."""
     import torch
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -199,6 +202,8 @@ def time_launches(launch, steps, stream, dist_mod, between=None):
     t1 = torch.cuda.Event(enable_timing=True)
     barrier(dist_mod)
     torch.cuda.synchronize()
+    if keep_ahead:
+        torch.cuda._sleep(min(2_000_000 + 20_000 * steps, 40_000_000))
     t0.record(stream)
     for i in range(steps):
         if between is not None:
@@ -293,6 +298,8 @@ def measure_variants(ops, wl, stream, dist_mod, peaks, steps, only=None, warm=5)
     import torch
     out = {}
     dev = torch.device("cuda")
+    if only in (None, "tile"):
+        out.update(_variant_tile(ops, wl, stream, dist_mod, steps, warm, dev))
     if only in (None, "small_m"):
         out.update(_variant_small_m(ops, wl, stream, dist_mod, peaks, steps, warm, dev))
     if only in (None, "square"):
@@ -300,6 +307,48 @@ def measure_variants(ops, wl, stream, dist_mod, peaks, steps, only=None, warm=5)
     if only in (None, "grouped"):
         out.update(_variant_grouped(ops, wl, stream, dist_mod, peaks, steps, warm, dev))
     return out
+
+
+def _variant_tile(ops, wl, stream, dist_mod, steps, warm, dev):
+    """The one-tile integer case (256x256x512, FP32 out): a latency figure."""
+    import torch
+    c = wl.tile_case()
+    A, B = c.A.to(dev), c.B.to(dev)
+    D = torch.empty((c.M, c.N), dtype=torch.float32, device=dev)
+    launch = dense_launcher(ops, A, B, D, wl.OUT_FP32, stream)
+    for _ in range(warm):
+        launch()
+    _, per = time_launches(launch, steps, stream, dist_mod, keep_ahead=True)
+    check_device_error(ops)
+    return {"tile_256x256x512_fp32out": {"ms_per_launch_median": statistics.median(per),
+                                         "ms_per_launch_min": min(per),
+                                         "note": "one CTA pair; launch latency dominates"}}
+
+
+def cublas_context(ops, stream, dev, reps=40):
+    """torch.matmul (cuBLAS) on the benchmark workload, launches alternated
+    with ours in blocks of 10, medians of CUDA-event times: context for the
+    roofline fraction, not part of the measured path."""
+    import torch
+    from blackwell_tensor_core_gb300 import workloads as wl
+    c = wl.large_case()
+    A, B = c.A.to(dev), c.B.to(dev)
+    D = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=dev)
+    D2 = torch.empty_like(D)
+    ours = dense_launcher(ops, A, B, D, wl.OUT_BF16, stream)
+    theirs = lambda: torch.matmul(A, B, out=D2)  # noqa: E731
+    for _ in range(3):
+        ours()
+        theirs()
+    to, tc = [], []
+    for _ in range(reps // 10):
+        to += time_launches(ours, 10, stream, None, keep_ahead=True)[1]
+        tc += time_launches(theirs, 10, stream, None, keep_ahead=True)[1]
+    check_device_error(ops)
+    mo, mc = statistics.median(to), statistics.median(tc)
+    return {"ours_ms_median": mo, "cublas_ms_median": mc, "ours_tflops": c.flops / (mo * 1e-3) / 1e12,
+            "cublas_tflops": c.flops / (mc * 1e-3) / 1e12, "ours_over_cublas": mc / mo,
+            "launches_each": len(to)}
 
 
 def _variant_small_m(ops, wl, stream, dist_mod, peaks, steps, warm, dev):
@@ -312,7 +361,7 @@ def _variant_small_m(ops, wl, stream, dist_mod, peaks, steps, warm, dev):
     launch = dense_launcher(ops, A, B, D, wl.OUT_BF16, stream)
     for _ in range(warm):
         launch()
-    _, per = time_launches(launch, steps, stream, dist_mod)
+    _, per = time_launches(launch, steps, stream, dist_mod, keep_ahead=True)
     check_device_error(ops)
     ms = statistics.mean(per)
     nbytes = 2 * (c.M * c.K + c.K * c.N + c.M * c.N)
@@ -494,6 +543,10 @@ def run_ours(args, rank, world, local):
     if not args.no_variants:
         variants = measure_variants(ops, wl, stream, dist_mod, peaks, min(args.steps, 200))
 
+    context = None
+    if not args.no_variants:
+        context = cublas_context(ops, stream, dev)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(case)
@@ -526,6 +579,7 @@ def run_ours(args, rank, world, local):
                       "first_tenth_mean": statistics.mean(per[:max(1, len(per) // 10)]),
                       "last_tenth_mean": statistics.mean(per[-max(1, len(per) // 10):])},
         "variants": variants,
+        "context_cublas": context,
     }
     print(json.dumps(line), flush=True)
 
@@ -540,7 +594,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--size", type=int, default=None,
                     help="square size of the timed GEMM (default 8192; smaller only for profiling)")
-    ap.add_argument("--only", choices=["small_m", "square", "grouped"], default=None,
+    ap.add_argument("--only", choices=["tile", "small_m", "square", "grouped"], default=None,
                     help="profiling aid: run only one variant workload, print its numbers")
     args = ap.parse_args(argv)
     if args.warmup < 3:
