@@ -62,6 +62,7 @@ struct DeviceState {
   int clusters_grouped_2c = 0;
   int ctas_1cta = 0;
   int clusters_grouped = 0;
+  int clusters_small[kMaxSplit + 1] = {};  // co-resident clusters of F small-M CTAs, F = 2..8
   // host-buffer entry point: copy streams and chunk events, made on first use
   bool host_ready = false;
   cudaStream_t h2d = nullptr, d2h = nullptr;
@@ -222,9 +223,34 @@ int no_tail_split_from_env() {
   return (v != nullptr && v[0] == '1') ? 1 : 0;
 }
 
+// Cluster split of the small-M kernel for few tiles: the cluster size F (2..8)
+// that keeps the most SMs streaming, with every cluster co-resident
+// (T <= clusters[F]) and at least two k-blocks per CTA; 1 if none helps.
+// clusters == nullptr: a host-side estimate (76, 36 and 15 co-resident
+// clusters of 2, 4 and 8 on 152 SMs, scaled to sm_count).
+int small_m_split(int T, int kb, int sm_count, const int* clusters) {
+  if (2 * T > sm_count) return 1;
+  int best = 1;
+  long long best_ctas = T;
+  for (int f = 2; f <= kMaxSplit; ++f) {
+    int c = 0;
+    if (clusters != nullptr)
+      c = clusters[f];
+    else if (f == 2 || f == 4 || f == 8)
+      c = (f == 2 ? sm_count / 2 : f == 4 ? sm_count * 36 / 152 : sm_count * 15 / 152);
+    if (c < T || kb < 2 * f) continue;
+    if (static_cast<long long>(T) * f > best_ctas) {
+      best_ctas = static_cast<long long>(T) * f;
+      best = f;
+    }
+  }
+  return best;
+}
+
 bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_count, int max_smem,
                       int force_kernel, int force_stages, int max_clusters_2cta, int max_ctas_1cta,
-                      int max_clusters_mc, int max_clusters_2c, bwg_plan_info* o) {
+                      int max_clusters_mc, int max_clusters_2c, bwg_plan_info* o,
+                      const int* small_clusters = nullptr) {
   std::memset(o, 0, sizeof(*o));
   if (M == 0 || N == 0) {
     o->kernel = BWG_KERNEL_NONE;
@@ -282,11 +308,28 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     // Stream-K pays when whole tiles would need a partly filled second wave,
     // or fill at most half the SMs; in between, whole tiles walking K in step
     // measured faster.
+    // With at most half the SMs' worth of tiles, a cluster split of K keeps
+    // more SMs streaming and sums the partials on chip (BWG_SMALL_M_SPLIT=0
+    // turns it off, =F forces cluster size F where it is valid; BWG_STREAMK=1
+    // takes stream-K instead).
+    int split = o->tile_n == 128 ? small_m_split(o->tiles, o->k_blocks, sm_count, small_clusters) : 1;
+    if (const char* v = std::getenv("BWG_SMALL_M_SPLIT")) {
+      const int f = std::atoi(v);
+      split = (f >= 2 && f <= kMaxSplit && o->tile_n == 128 && o->k_blocks >= 2 * f) ? f : 1;
+    }
     int streamk = (o->tiles % sm_count != 0 && (o->tiles > sm_count || 2 * o->tiles <= sm_count) &&
-                   iters >= sm_count) ? 1 : 0;
-    if (const char* v = std::getenv("BWG_STREAMK")) streamk = (v[0] == '1' && iters >= sm_count) ? 1 : 0;
+                   iters >= sm_count && split == 1) ? 1 : 0;
+    if (const char* v = std::getenv("BWG_STREAMK")) {
+      streamk = (v[0] == '1' && iters >= sm_count) ? 1 : 0;
+      if (streamk) split = 1;
+    }
+    // each CTA's partial and the rows it receives fit in its idle stage ring
+    if (split > 1 && (static_cast<long long>(m_pad) + static_cast<long long>(split) * ceil_div(M, split)) * 512 >
+                         static_cast<long long>(stages) * small_m_stage_bytes(m_pad))
+      split = 1;
     o->streamk = streamk;
-    o->grid = streamk ? sm_count : std::min(o->tiles, sm_count);
+    o->split = split;
+    o->grid = streamk ? sm_count : split > 1 ? o->tiles * split : std::min(o->tiles, sm_count);
     o->tx_bytes = static_cast<uint32_t>(small_m_stage_bytes(m_pad));
     o->idesc = make_idesc_f16(fmt, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, m_pad);
   } else {
@@ -457,6 +500,10 @@ bwg_status ensure_device(DeviceState** out) {
         if (st.clusters_grouped_2c <= 0) st.clusters_grouped_2c = st.sm_count / 2;
         if (st.clusters_grouped <= 0) st.clusters_grouped = st.sm_count / 2;
         if (st.ctas_1cta <= 0) st.ctas_1cta = st.sm_count;
+        // every small-M configuration takes more than half an SM's shared
+        // memory, so one query at the largest size holds for all of them
+        for (int f = 2; f <= kMaxSplit; ++f)
+          st.clusters_small[f] = max_active_clusters_small_m(f, static_cast<size_t>(st.max_smem));
       }
     }
   }
@@ -539,7 +586,7 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
   bwg_plan_info pl;
   s = plan_dense(M, N, K, out_dtype, fp16_in, st->sm_count, st->max_smem, force_kernel_from_env(),
                  force_stages_from_env(), st->clusters_2cta, st->ctas_1cta, st->clusters_mc,
-                 st->clusters_2c, &pl);
+                 st->clusters_2c, &pl, st->clusters_small);
   if (s != BWG_OK) return s;
   if (pl.kernel == BWG_KERNEL_ZERO)
     return launch_status(launch_zero_fill(D, M, N, ldd, out_elt(out_dtype), stream));
@@ -575,6 +622,9 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
     p.idesc = pl.idesc;
     p.tx_extra = g_tx_extra.load();
     p.streamk = pl.streamk;
+    p.split = pl.split;
+    p.d = D;
+    p.ldd = ldd;
     p.trace = g_trace.load();
     if (pl.streamk) {
       p.ws_slots = streamk_max_sharers(pl.tiles, pl.k_blocks, pl.grid);

@@ -34,6 +34,16 @@
 // sharers sums the slots in slot order (deterministic), stores D and resets
 // the counter.  No CTA ever waits for another.  With stream-K off, segments
 // are whole tiles taken persistently (tile = CTA index + i * grid).
+//
+// Cluster split (few tiles, split > 1): a cluster of `split` CTAs shares one
+// tile's k-blocks in equal slices.  When every CTA of the cluster has
+// finished its MMAs, all their stage rings are idle; each CTA writes its FP32
+// partial into its own ring and bulk-copies the rows that CTA o finishes
+// (rows o*ceil(M/split) ..) into o's ring through distributed shared memory,
+// counted on o's barrier; each CTA then sums the `split` partials of its rows
+// in rank order and stores them.  The partials never leave the chip and no workspace is needed; CTAs
+// of one cluster are co-scheduled, so waiting for one another is safe (the
+// waits are bounded all the same).
 #include "layout.h"
 #include "params.h"
 #include "ptx.cuh"
@@ -68,6 +78,15 @@ struct Segments {
 
   // Segment i: false when there is none.
   __device__ bool get(int i, int* t, int* kb0, int* kb1) const {
+    if (p.split > 1) {
+      // one slice of one tile: clusters are formed from consecutive CTAs
+      if (i > 0) return false;
+      const int r = static_cast<int>(blockIdx.x) % p.split;
+      *t = static_cast<int>(blockIdx.x) / p.split;
+      *kb0 = (p.num_k_blocks * r) / p.split;
+      *kb1 = (p.num_k_blocks * (r + 1)) / p.split;
+      return true;
+    }
     if (!p.streamk) {
       const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
       if (tile >= p.num_tiles) return false;
@@ -115,6 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
   auto acc_empty_bar = [&](int a) { return smem_bar + 8u * (2 * S + 2 + a); };
   const uint32_t tmem_slot = smem_bar + 8u * (2 * S + 4);
   const uint32_t last_flag = tmem_slot + 4u;  // "this CTA finishes the tile" broadcast
+  const uint32_t ready_bar = tmem_slot + 8u;   // split: every CTA of the cluster has its partial
+  const uint32_t recv_bar = tmem_slot + 16u;   // split: the other CTAs' rows have landed here
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -125,6 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
       mbar_init(acc_full_bar(a), 1);
       mbar_init(acc_empty_bar(a), 4);
     }
+    mbar_init(ready_bar, static_cast<uint32_t>(p.split > 1 ? p.split : 1));
+    mbar_init(recv_bar, 1);
     fence_mbarrier_init();
     prefetch_tensormap(&p.map_bt);
     prefetch_tensormap(&p.map_at);
@@ -188,7 +211,11 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
     tmem_relinquish<1>();
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  if (p.split > 1)
+    cluster_sync_all();  // the cluster's barriers are initialised before any remote arrival
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = ld_shared_u32(tmem_slot);
 
@@ -309,6 +336,99 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
       }
       tc_fence_after();
       if (trace != nullptr && store_thread) trace[4] = globaltimer_ns();
+      if (p.split > 1) {
+        const int F = p.split;
+        const uint32_t me = cluster_ctarank();
+        const uint32_t t_acc = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc) * 256u;
+        const int rpc = (p.M + F - 1) / F;  // rows each CTA finishes
+        const int my_rows = max(0, min(rpc, p.M - static_cast<int>(me) * rpc));
+        const uint32_t slot_bytes = static_cast<uint32_t>(rpc) * 512u;  // [rpc][128] FP32
+        // 1. This CTA's partial is complete: count the rows it will receive,
+        //    then tell every CTA of the cluster (itself included).
+        if (store_thread) {
+          mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(F - 1) * static_cast<uint32_t>(my_rows) * 512u);
+          for (int r = 0; r < F; ++r) mbar_arrive_cluster(mapa_shared(ready_bar, static_cast<uint32_t>(r)));
+        }
+        // 2. When all have, every stage ring of the cluster is idle.
+        const bool ready = mbar_wait(ready_bar, 0, p.timeout_ns);
+        if (!named_bar_and(1, 128, ready)) {
+          if (store_thread) record_fault_small(p.err, 2, 5, 0, 0);
+          aborted = true;
+          break;
+        }
+        if (trace != nullptr && store_thread) trace[5] = globaltimer_ns();
+        // 3. The partial goes to this CTA's idle ring as [M rows][128] FP32
+        //    (a warp writes 128 contiguous bytes of a row); then one thread
+        //    bulk-copies rows [o*rpc, o*rpc + rows_o) to slot `me` of each
+        //    other CTA o, counted on o's receive barrier.
+#pragma unroll 1
+        for (int c0 = 0; c0 < p.m_pad; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(t_acc + c0, v);
+          tmem_wait_ld();
+          const int n = min(16, p.M - c0);
+          const uint32_t a = base + static_cast<uint32_t>(c0) * 512u + ch * 4u;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j < n) st_shared_u32(a + j * 512u, v[j]);
+        }
+        fence_proxy_async_shared();
+        named_bar_sync(1, 128);
+        const uint32_t recv = base + static_cast<uint32_t>(p.m_pad) * 512u;  // F slots of rpc rows
+        if (store_thread) {
+          for (int o = 0; o < F; ++o) {
+            const int rows_o = min(rpc, p.M - o * rpc);
+            if (o == static_cast<int>(me) || rows_o <= 0) continue;
+            bulk_copy_to_cluster(mapa_shared(recv + me * slot_bytes, static_cast<uint32_t>(o)),
+                                 base + static_cast<uint32_t>(o * rpc) * 512u,
+                                 static_cast<uint32_t>(rows_o) * 512u,
+                                 mapa_shared(recv_bar, static_cast<uint32_t>(o)));
+          }
+        }
+        if (trace != nullptr && store_thread) trace[6] = globaltimer_ns();
+        // 4. Wait for the other CTAs' rows of this CTA.
+        const bool got = mbar_wait(recv_bar, 0, p.timeout_ns);
+        if (!named_bar_and(1, 128, got)) {
+          if (store_thread) record_fault_small(p.err, 2, 6, 0, 0);
+          aborted = true;
+          break;
+        }
+        if (trace != nullptr && store_thread) trace[7] = globaltimer_ns();
+        // 5. Sum the partials in rank order (this CTA's own from its local
+        //    copy) and store this CTA's rows of D, four rows at a time so the
+        //    shared-memory loads of a row group are independent.
+        const int col = n0 + static_cast<int>(ch);
+        if (stores && col < p.N) {
+          const int r0 = static_cast<int>(me) * rpc;
+          const float* own = reinterpret_cast<const float*>(smem_raw + (base - smem_u32(smem_raw))) +
+                             static_cast<size_t>(r0) * 128u + ch;
+          const float* slots = reinterpret_cast<const float*>(smem_raw + (recv - smem_u32(smem_raw))) + ch;
+          const size_t ldd = static_cast<size_t>(p.ldd);
+#pragma unroll 1
+          for (int r = 0; r < my_rows; r += 4) {
+            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+            for (int src = 0; src < F; ++src) {
+              const float* q4 = (src == static_cast<int>(me) ? own : slots + static_cast<size_t>(src) * rpc * 128u) +
+                                static_cast<size_t>(r) * 128u;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (r + j < my_rows) sum[j] += q4[j * 128];
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (r + j < my_rows) {
+                const size_t at = static_cast<size_t>(r0 + r + j) * ldd + col;
+                if (out32)
+                  static_cast<float*>(p.d)[at] = sum[j];
+                else
+                  static_cast<uint16_t*>(p.d)[at] = outbf ? cvt_rn_bf16(sum[j]) : cvt_rn_f16(sum[j]);
+              }
+            }
+          }
+        }
+        break;  // a split CTA has one segment
+      }
       // The previous TMA store must have finished reading the staging tile.
       if (store_thread) bulk_wait_group_read<0>();
       named_bar_sync(1, 128);
@@ -437,8 +557,44 @@ __global__ void zero_fill_kernel(uint8_t* d, int rows, int row_bytes, size_t ld_
 }  // namespace
 
 cudaError_t launch_small_m(const SmallMParams& p, int grid, size_t smem, cudaStream_t s) {
-  small_m_kernel<<<grid, kThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  if (p.split <= 1) {
+    small_m_kernel<<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.split);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, small_m_kernel, p);
+}
+
+int max_active_clusters_small_m(int cluster, size_t smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(small_m_kernel), &cfg) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 cudaError_t launch_zero_fill(void* d, int rows, int cols, int ld, int elt_bytes, cudaStream_t s) {

@@ -18,6 +18,7 @@ constexpr int kEpiBytes = 4 * 2 * kEpiBufBytes;  // 4 epilogue warps, double-buf
 constexpr uint32_t kTmemCols = 512;  // two 256-column FP32 accumulators
 constexpr int kMaxGroupsPerLaunch = 64;
 constexpr int kSmallMMaxM = 128;     // swapped kernel handles up to 128 rows of A
+constexpr int kMaxSplit = 8;         // largest cluster of the small-M split (portable size)
 
 // Output element type codes (same values as the C ABI).
 constexpr int kOutBF16 = 0;
@@ -92,6 +93,13 @@ struct SmallMParams {
   int ws_slots;      // partial-accumulator slots per tile (most CTAs sharing a tile)
   float* ws;         // stream-K partials: [num_tiles][ws_slots][m_pad][128] FP32
   int* ws_counters;  // stream-K arrival counters, one per tile, zero between calls
+  // Cluster split of K (split > 1): the grid is num_tiles clusters of `split`
+  // CTAs; CTA r of cluster t computes k-blocks [r*kb/split, (r+1)*kb/split) of
+  // tile t, and the cluster sums its partials through distributed shared
+  // memory, each CTA finishing ceil(M/split) rows of D, which it stores itself.
+  int split;
+  void* d;            // D (split mode stores its rows directly)
+  long long ldd;      // D's leading dimension, elements
   // Optional trace (nullptr: off): per CTA eight global-timer stamps (ns),
   // documented with bwg_debug_set_trace.
   unsigned long long* trace;
@@ -112,6 +120,8 @@ int max_active_clusters_grouped_2c(size_t smem);
 cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, cudaStream_t s,
                                 bool swiglu = false);
 cudaError_t launch_small_m(const SmallMParams& p, int grid, size_t smem, cudaStream_t s);
+// Co-resident clusters of `cluster` small-M CTAs with `smem` bytes each (0 on error).
+int max_active_clusters_small_m(int cluster, size_t smem);
 cudaError_t launch_zero_fill(void* d, int rows, int cols, int ld, int elt_bytes, cudaStream_t s);
 
 // Probe kernels (test hooks, probes.cu).

@@ -234,6 +234,24 @@ BWG_DEV void bulk_wait_group() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Bulk copy of `bytes` (multiple of 16, 16-byte aligned) from this CTA's
+// shared memory to the shared memory of a CTA of the cluster (`dst` and
+// `bar` are shared::cluster addresses of that CTA, e.g. from mapa_shared),
+// completing the bytes on that CTA's barrier.
+BWG_DEV void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+BWG_DEV float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA store, tcgen05.mma operand reads).
 BWG_DEV void fence_proxy_async_shared() {

@@ -281,6 +281,10 @@ typedef struct {
   int sk_tiles;            /* 2CTA_2C: tiles of the last wave shared out by k-block over
                               all pairs (stream-K; streamk = 1), 0 if none */
   int sk_segs;             /* 2CTA_2C stream-K: most segments in one pair's range */
+  int split;               /* SMALL_M: CTAs of a cluster that share each tile's k-blocks in
+                              equal slices and sum their FP32 partials through
+                              distributed shared memory (grid = tiles x split); 1 if
+                              none.  Taken when the tiles fill at most half the SMs */
 } bwg_plan_info;
 
 /*

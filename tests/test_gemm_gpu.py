@@ -309,6 +309,51 @@ def test_small_m_streamk_bf16_bound_and_growing_workspace(monkeypatch):
         assert_within_bound(D, Dref, S, "streamk %s" % ((M, N, K),))
 
 
+@pytest.mark.parametrize("shape", [(72, 4096, 7168), (70, 1000, 4096), (3, 640, 2048), (128, 4104, 640),
+                                   (16, 2048, 4136), (72, 7168, 2048), (33, 312, 1016)])
+def test_small_m_cluster_split_exact(shape, monkeypatch):
+    """Cluster split of K (partials summed through distributed shared memory):
+    exact on integer inputs for every output type, with ragged M (rows not a
+    multiple of the cluster, fewer rows than CTAs), ragged K and N, and the
+    same bits on every repeat; equal to the unsplit and stream-K results."""
+    from blackwell_tensor_core_gb300 import ops
+    M, N, K = shape
+    pl = ops.plan(M, N, K)
+    assert pl.split > 1, (shape, pl.split)
+    g = wl.generator(5750 + M + N)
+    A = wl.randint_matrix(M, K, -2, 2, g)
+    B = wl.randint_matrix(K, N, -2, 2, g)
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+    for _ in range(2):
+        D, _ = gpu_gemm(A, B, wl.OUT_FP32, None)
+        assert np.array_equal(D.double().numpy(), Dref)
+    D16, _ = gpu_gemm(A, B, wl.OUT_BF16, None)
+    assert_bits_equal(D16, oracle.round_to(Dref, "bf16"), "split bf16 %s" % (shape,))
+    Ah, Bh = A.to(torch.float16), B.to(torch.float16)
+    Dh, _ = gpu_gemm(Ah, Bh, wl.OUT_FP16, None)
+    assert_bits_equal(Dh, oracle.round_to(Dref, "fp16"), "split fp16 %s" % (shape,))
+    monkeypatch.setenv("BWG_SMALL_M_SPLIT", "0")
+    D0, _ = gpu_gemm(A, B, wl.OUT_FP32, None)
+    assert np.array_equal(D0.double().numpy(), Dref)
+
+
+def test_small_m_cluster_split_random_bound_and_padding():
+    """Random inputs within the bound, bit-identical run to run, and a padded
+    leading dimension of D left untouched."""
+    from blackwell_tensor_core_gb300 import ops
+    M, N, K = 72, 4096, 7168
+    assert ops.plan(M, N, K).split == 4
+    g = wl.generator(5790)
+    A = wl.normal_matrix(M, K, 0.02, g)
+    B = wl.normal_matrix(K, N, 0.02, g)
+    D1, full = gpu_gemm(A, B, wl.OUT_BF16, None, ldd=N + 64, sentinel=7.0)
+    D2, _ = gpu_gemm(A, B, wl.OUT_BF16, None, ldd=N + 64, sentinel=7.0)
+    assert torch.equal(D1, D2)
+    assert (full[:, N:] == 7.0).all()
+    Dref, S = oracle.gemm(wl.bits(A), wl.bits(B))
+    assert_within_bound(D1, Dref, S, "split random")
+
+
 def test_small_m_streamk_on_a_side_stream():
     from blackwell_tensor_core_gb300 import ops
     g = wl.generator(5700)

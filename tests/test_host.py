@@ -164,8 +164,8 @@ def test_planner_choices(ops):
     assert small.kernel == ops.KERNEL_SMALL_M and small.mma_n == 80
     # whole 128-column tiles walking K in step; stream-K for few or too many tiles
     assert small.tile_n == 128 and small.tiles == 128 and small.streamk == 0 and small.grid == 128
-    assert ops.plan(72, 8192, 7168).streamk == 1 and ops.plan(72, 24576, 7168).streamk == 1
-    assert ops.plan(72, 19456, 7168).streamk == 0
+    assert ops.plan(72, 24576, 7168).streamk == 1 and ops.plan(72, 19456, 7168).streamk == 0
+    assert small.split == 1
     assert small.smem_total <= 232448 and small.stages >= 4
     for tokens, n in _golden()["n_compute"]:
         assert ops.plan(int(tokens), 4096, 4096).mma_n == n
@@ -176,6 +176,28 @@ def test_planner_choices(ops):
     assert p2.smem_input_per_cta // 2 == 48 * 1024  # two A blocks + one B block per CTA per stage
     assert p2.tx_bytes == 2 * 48 * 1024
     assert ops.plan(128, 10, 10).kernel == ops.KERNEL_SMALL_M
+
+
+def test_small_m_cluster_split_plan(ops, monkeypatch):
+    """Few column tiles (at most half the SMs): a cluster of F CTAs shares
+    each tile's k-blocks, F chosen to keep the most SMs streaming with every
+    cluster co-resident (host estimate: 76, 36, 15 clusters of 2, 4, 8 on 152
+    SMs) and at least two k-blocks per CTA."""
+    cases = {(72, 4096, 7168): 4, (72, 8192, 7168): 2, (72, 7168, 2048): 2, (72, 1000, 4096): 8,
+             (16, 2048, 4096): 4, (128, 4104, 640): 4, (72, 16384, 7168): 1, (72, 256, 64): 1,
+             (72, 24576, 7168): 1, (72, 1000, 448): 2}
+    for shape, F in cases.items():
+        p = ops.plan(*shape)
+        assert p.split == F, (shape, p.split)
+        if F > 1:
+            assert p.streamk == 0 and p.grid == p.tiles * F and p.k_blocks >= 2 * F
+    monkeypatch.setenv("BWG_SMALL_M_SPLIT", "0")
+    assert ops.plan(72, 4096, 7168).split == 1 and ops.plan(72, 4096, 7168).streamk == 1
+    monkeypatch.setenv("BWG_SMALL_M_SPLIT", "2")
+    assert ops.plan(72, 4096, 7168).split == 2
+    monkeypatch.delenv("BWG_SMALL_M_SPLIT")
+    monkeypatch.setenv("BWG_STREAMK", "1")
+    assert ops.plan(72, 4096, 7168).split == 1 and ops.plan(72, 4096, 7168).streamk == 1
 
 
 def test_instruction_descriptor_words(ops):
