@@ -56,9 +56,12 @@ typedef enum { BWG_OUT_BF16 = 0, BWG_OUT_FP32 = 1, BWG_OUT_FP16 = 2 } bwg_out_dt
  *   lda >= K, ldb >= N, ldd >= N.  M, N or K == 0: M or N == 0 is a no-op;
  *   K == 0 writes D = 0.  Sizes above 2^31-1 elements per dimension are not
  *   supported.  Returns BWG_OK once the work is enqueued.
- *   The small-M kernel may share a tile's k-blocks among several CTAs; it then
- *   uses a device workspace that the library allocates (cudaMalloc) on the
- *   first such call on a stream and keeps for later calls on that stream.
+ *   The small-M kernel may share a tile's k-blocks among several CTAs.  With
+ *   few column tiles (at most half the SMs' worth) the CTAs form clusters and
+ *   sum their partials in shared memory; with more tiles than SMs and a ragged
+ *   last wave they share k-blocks stream-K style through a device workspace
+ *   that the library allocates (cudaMalloc) on the first such call on a
+ *   stream and keeps for later calls on that stream.
  */
 bwg_status gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K, int lda, int ldb,
                      int ldd, int out_dtype, void* stream);
