@@ -243,6 +243,24 @@ void bwg_debug_set_tx_extra(unsigned int bytes);
 void bwg_debug_set_trace(void* buffer);
 
 /* ---------------------------------------------------------------------
+ * Planner overrides (environment variables, read on every call; for
+ * experiments and tests -- the defaults are the measured best):
+ *   BWG_FORCE_KERNEL   1cta | 2cta | 2cta_mc | 2cta_2c | small_m: kernel kind
+ *   BWG_FORCE_STAGES   ring depth (must fit the shared memory)
+ *   BWG_EPILOGUE       direct: pair kernels store D from registers (default tma)
+ *   BWG_GROUP_M        tile rows per raster group (default 8)
+ *   BWG_SCHED          clc | static: two-consumer scheduling (default: clc for
+ *                      grouped, static for dense)
+ *   BWG_NO_TAIL_SPLIT  1: no last-wave cut
+ *   BWG_STREAMK_DENSE  1: stream-K last wave in the dense two-consumer kernel
+ *   BWG_SMALL_M_TILE_N output columns per small-M tile (16..128, default 128)
+ *   BWG_SMALL_M_SPLIT  0: no cluster split; F (2..8): that cluster size
+ *   BWG_STREAMK        1 / 0: force stream-K on / off in the small-M kernel
+ *   BWG_GROUPED_1C     1: grouped kernels with one MMA consumer (256-row units)
+ *   BWG_GROUPED_SWAP   1: swapped-operand group ends (one-consumer grouped kernel)
+ * ------------------------------------------------------------------- */
+
+/* ---------------------------------------------------------------------
  * Host-only planning and layout helpers (no GPU needed; used by tests).
  * ------------------------------------------------------------------- */
 
