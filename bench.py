@@ -539,8 +539,18 @@ def run_ours(args, rank, world, local):
     del hA, hB, hD
 
     variants = None
+    variant_clocks = None
     if not args.no_variants:
+        vs = ClockSampler(torch.cuda.current_device())
+        vs.start()
         variants = measure_variants(ops, wl, stream, dist_mod, peaks, min(args.steps, 200))
+        variant_clocks = vs.stop()
+        # the variants run right after the long timed loop, at the power cap:
+        # give their fractions of the sustained figure too
+        for v in variants.values():
+            r = v.get("roofline")
+            if r and r.get("unit") == "TFLOP/s":
+                r["frac_of_sustained"] = r["achieved"] / peaks["bf16_tflops_sustained"]
 
     context = None
     if not args.no_variants:
@@ -580,6 +590,7 @@ def run_ours(args, rank, world, local):
                       "first_tenth_mean": statistics.mean(per[:max(1, len(per) // 10)]),
                       "last_tenth_mean": statistics.mean(per[-max(1, len(per) // 10):])},
         "variants": variants,
+        "variants_clocks": variant_clocks,
         "context_cublas": context,
     }
     print(json.dumps(line), flush=True)
