@@ -52,6 +52,40 @@ def test_stalled_stage_barrier_times_out_and_context_survives(kind, M, sched, mo
     assert np.array_equal(Dg.double().numpy(), Dref)
 
 
+@pytest.mark.parametrize("mode,K", [("split", 256), ("whole", 256), ("streamk", 4864)])
+def test_small_m_modes_time_out_and_context_survives(mode, K, monkeypatch):
+    """The small-M kernel in each of its work splits -- cluster split (CTAs
+    of a cluster also wait for each other's partials), whole tiles, and
+    stream-K -- gives up on a stage barrier that cannot complete, reports
+    BWG_ERR_TIMEOUT, and the next call is exact."""
+    from blackwell_tensor_core_gb300 import ops
+    M, N = 64, 256
+    if mode == "whole":
+        monkeypatch.setenv("BWG_SMALL_M_SPLIT", "0")
+    if mode == "streamk":
+        monkeypatch.setenv("BWG_STREAMK", "1")
+    pl = ops.plan(M, N, K)
+    assert (pl.split > 1) == (mode == "split") and (pl.streamk == 1) == (mode == "streamk")
+    g = wl.generator(7050 + K)
+    A = wl.randint_matrix(M, K, -2, 2, g)
+    B = wl.randint_matrix(K, N, -2, 2, g)
+    Ad, Bd = A.cuda(), B.cuda()
+    D = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    ops.set_watchdog_ns(50_000_000)  # 50 ms
+    ops.debug_set_tx_extra(1024)
+    try:
+        ops.gemm_bf16(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K, K, N, N, wl.OUT_FP32,
+                      torch.cuda.current_stream().cuda_stream)
+        st, word = ops.last_device_error()
+    finally:
+        ops.debug_set_tx_extra(0)
+        ops.set_watchdog_ns(0)
+    assert st == 5 and (word >> 56) == 1, (st, hex(word))
+    Dg, _ = gpu_gemm(A, B, wl.OUT_FP32, None)
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+    assert np.array_equal(Dg.double().numpy(), Dref)
+
+
 @pytest.mark.parametrize("sched", ["clc", "static"])
 def test_grouped_stalled_stage_barrier_times_out(sched, monkeypatch):
     """The grouped two-consumer kernel (dynamic and static scheduling) gives
