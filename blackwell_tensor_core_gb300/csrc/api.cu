@@ -193,8 +193,11 @@ int small_m_stage_bytes(int m_pad) { return 128 * kBK * 2 + m_pad * kBK * 2; }
 
 int small_m_staging(int m_pad, int out_dtype) { return 2 * m_pad * 64 * (out_dtype == kOutF32 ? 4 : 2); }
 
-int small_m_smem(int m_pad, int out_dtype, int stages) {
-  return 1024 + stages * small_m_stage_bytes(m_pad) + 1024 + small_m_staging(m_pad, out_dtype) + 512;
+// Dynamic shared memory of the small-M kernel: alignment slack, the stage
+// ring, the output staging tile (unless it lives in the ring), barriers.
+int small_m_smem(int m_pad, int out_dtype, int stages, bool staging_in_ring = false) {
+  return 1024 + stages * small_m_stage_bytes(m_pad) +
+         (staging_in_ring ? 0 : 1024 + small_m_staging(m_pad, out_dtype)) + 512;
 }
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
@@ -250,7 +253,7 @@ int small_m_split(int T, int kb, int sm_count, const int* clusters) {
 bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_count, int max_smem,
                       int force_kernel, int force_stages, int max_clusters_2cta, int max_ctas_1cta,
                       int max_clusters_mc, int max_clusters_2c, bwg_plan_info* o,
-                      const int* small_clusters = nullptr) {
+                      const int* small_clusters = nullptr, bool force_streamk = false) {
   std::memset(o, 0, sizeof(*o));
   if (M == 0 || N == 0) {
     o->kernel = BWG_KERNEL_NONE;
@@ -288,13 +291,6 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     o->tile_n = 128;
     o->mma_m = 128;
     o->mma_n = m_pad;
-    const int fixed = small_m_smem(m_pad, out_dtype, 0);
-    int stages = std::min(8, (max_smem - fixed) / small_m_stage_bytes(m_pad));
-    if (force_stages > 0) stages = force_stages;
-    if (stages < 2 || small_m_smem(m_pad, out_dtype, stages) > max_smem) return BWG_ERR_UNSUPPORTED;
-    o->stages = stages;
-    o->smem_input_per_cta = stages * small_m_stage_bytes(m_pad);
-    o->smem_total = small_m_smem(m_pad, out_dtype, stages);
     // 128 columns per tile by default: narrower strides start B's boxes off a
     // 128-byte boundary, which measured slower than leaving SMs idle.
     int tn = 128;
@@ -305,9 +301,6 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     o->tile_n = tn;
     o->tiles = ceil_div(N, tn);
     const long long iters = static_cast<long long>(o->tiles) * o->k_blocks;
-    // Stream-K pays when whole tiles would need a partly filled second wave,
-    // or fill at most half the SMs; in between, whole tiles walking K in step
-    // measured faster.
     // With at most half the SMs' worth of tiles, a cluster split of K keeps
     // more SMs streaming and sums the partials on chip (BWG_SMALL_M_SPLIT=0
     // turns it off, =F forces cluster size F where it is valid; BWG_STREAMK=1
@@ -317,12 +310,30 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
       const int f = std::atoi(v);
       split = (f >= 2 && f <= kMaxSplit && o->tile_n == 128 && o->k_blocks >= 2 * f) ? f : 1;
     }
+    // Stream-K pays when whole tiles would need a partly filled second wave,
+    // or fill at most half the SMs; in between, whole tiles walking K in step
+    // measured faster.
     int streamk = (o->tiles % sm_count != 0 && (o->tiles > sm_count || 2 * o->tiles <= sm_count) &&
                    iters >= sm_count && split == 1) ? 1 : 0;
     if (const char* v = std::getenv("BWG_STREAMK")) {
       streamk = (v[0] == '1' && iters >= sm_count) ? 1 : 0;
       if (streamk) split = 1;
     }
+    if (force_streamk) {  // the no-allocation entry point: always stream-K
+      streamk = 1;
+      split = 1;
+    }
+    // With one tile per CTA the stage ring is idle when the epilogue runs, so
+    // the output staging tile lives in it and the ring gets one stage deeper.
+    const bool in_ring = !streamk && (split > 1 || o->tiles <= sm_count);
+    const int fixed = small_m_smem(m_pad, out_dtype, 0, in_ring);
+    int stages = std::min(8, (max_smem - fixed) / small_m_stage_bytes(m_pad));
+    if (force_stages > 0) stages = force_stages;
+    if (stages < 2 || small_m_smem(m_pad, out_dtype, stages, in_ring) > max_smem) return BWG_ERR_UNSUPPORTED;
+    o->stages = stages;
+    o->smem_input_per_cta = stages * small_m_stage_bytes(m_pad);
+    o->smem_total = small_m_smem(m_pad, out_dtype, stages, in_ring);
+    o->staging_in_ring = in_ring ? 1 : 0;
     // each CTA's partial and the rows it receives fit in its idle stage ring
     if (split > 1 && (static_cast<long long>(m_pad) + static_cast<long long>(split) * ceil_div(M, split)) * 512 >
                          static_cast<long long>(stages) * small_m_stage_bytes(m_pad))
@@ -623,6 +634,7 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
     p.tx_extra = g_tx_extra.load();
     p.streamk = pl.streamk;
     p.split = pl.split;
+    p.staging_in_ring = pl.staging_in_ring;
     p.d = D;
     p.ldd = ldd;
     p.trace = g_trace.load();
@@ -853,7 +865,7 @@ bwg_status run_small_m_noalloc(const void* A, const void* B, void* D, int M, int
   if (K == 0) return launch_status(launch_zero_fill(D, M, N, ldd, out_elt(out_dtype), stream));
   bwg_plan_info pl;
   s = plan_dense(M, N, K, out_dtype, false, st->sm_count, st->max_smem, BWG_KERNEL_SMALL_M, 0,
-                 st->clusters_2cta, st->ctas_1cta, st->clusters_mc, st->clusters_2c, &pl);
+                 st->clusters_2cta, st->ctas_1cta, st->clusters_mc, st->clusters_2c, &pl, nullptr, true);
   if (s != BWG_OK) return s;
   // Always the stream-K form: every CTA gets at least one k-block.
   const long long iters = static_cast<long long>(pl.tiles) * pl.k_blocks;

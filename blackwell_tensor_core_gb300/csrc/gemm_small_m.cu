@@ -126,8 +126,12 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
 
   const uint32_t smem_bt = base;
   const uint32_t smem_at = smem_bt + S * kBtStageBytes;
-  const uint32_t smem_d = (smem_at + S * at_stage_bytes + 1023u) & ~1023u;
-  const uint32_t smem_bar = (smem_d + 2u * half_bytes + 15u) & ~15u;
+  const uint32_t ring_end = smem_at + S * at_stage_bytes;
+  // output staging tile: in the ring when every CTA has a single tile (the
+  // ring is idle by the time the epilogue runs), else after it
+  const uint32_t smem_d = p.staging_in_ring ? base : ((ring_end + 1023u) & ~1023u);
+  const uint32_t smem_bar = p.staging_in_ring ? ((ring_end + 15u) & ~15u)
+                                              : ((smem_d + 2u * half_bytes + 15u) & ~15u);
   auto full_bar = [&](int s) { return smem_bar + 8u * s; };
   auto empty_bar = [&](int s) { return smem_bar + 8u * (S + s); };
   auto acc_full_bar = [&](int a) { return smem_bar + 8u * (2 * S + a); };

@@ -98,6 +98,7 @@ struct SmallMParams {
   // tile t, and the cluster sums its partials through distributed shared
   // memory, each CTA finishing ceil(M/split) rows of D, which it stores itself.
   int split;
+  int staging_in_ring;  // 1: one tile per CTA, the output staging tile sits in the idle ring
   void* d;            // D (split mode stores its rows directly)
   long long ldd;      // D's leading dimension, elements
   // Optional trace (nullptr: off): per CTA eight global-timer stamps (ns),

@@ -306,6 +306,9 @@ typedef struct {
                               equal slices and sum their FP32 partials through
                               distributed shared memory (grid = tiles x split); 1 if
                               none.  Taken when the tiles fill at most half the SMs */
+  int staging_in_ring;     /* SMALL_M: 1 if every CTA has one tile (or one slice of one
+                              tile), so the output staging tile reuses the stage ring,
+                              idle by then, and the ring is one stage deeper */
 } bwg_plan_info;
 
 /*
