@@ -253,7 +253,8 @@ int small_m_split(int T, int kb, int sm_count, const int* clusters) {
 bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_count, int max_smem,
                       int force_kernel, int force_stages, int max_clusters_2cta, int max_ctas_1cta,
                       int max_clusters_mc, int max_clusters_2c, bwg_plan_info* o,
-                      const int* small_clusters = nullptr, bool force_streamk = false) {
+                      const int* small_clusters = nullptr, bool force_streamk = false,
+                      bool b_kmajor = false) {
   std::memset(o, 0, sizeof(*o));
   if (M == 0 || N == 0) {
     o->kernel = BWG_KERNEL_NONE;
@@ -342,7 +343,7 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     o->split = split;
     o->grid = streamk ? sm_count : split > 1 ? o->tiles * split : std::min(o->tiles, sm_count);
     o->tx_bytes = static_cast<uint32_t>(small_m_stage_bytes(m_pad));
-    o->idesc = make_idesc_f16(fmt, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, m_pad);
+    o->idesc = make_idesc_f16(fmt, /*a_mn_major=*/!b_kmajor, /*b_mn_major=*/false, 128, m_pad);
   } else {
     const int cg = (kind == BWG_KERNEL_1CTA) ? 1 : 2;
     const int mc = (kind == BWG_KERNEL_2CTA_MC) ? 2 : 1;  // pairs per cluster
@@ -376,7 +377,7 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
       o->grid = o->workers;
     }
     o->tx_bytes = static_cast<uint32_t>(cg * dense_stage_bytes(cg, nc));
-    o->idesc = make_idesc_f16(fmt, /*a_mn_major=*/false, /*b_mn_major=*/true, o->mma_m, kTileN);
+    o->idesc = make_idesc_f16(fmt, /*a_mn_major=*/false, /*b_mn_major=*/!b_kmajor, o->mma_m, kTileN);
   }
   o->coverage = static_cast<double>(M) * N / (static_cast<double>(o->tiles) * o->tile_m * o->tile_n);
   o->units = o->tiles;
@@ -430,14 +431,16 @@ int out_elt(int out_dtype) { return out_dtype == BWG_OUT_FP32 ? 4 : 2; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// b_kmajor: B is stored [N, K] (ldb >= K) instead of [K, N] (ldb >= N).
 bwg_status check_args(const void* A, const void* B, const void* D, int M, int N, int K, int lda,
-                      int ldb, int ldd, int out_dtype) {
+                      int ldb, int ldd, int out_dtype, bool b_kmajor = false) {
   if (out_dtype != BWG_OUT_BF16 && out_dtype != BWG_OUT_FP32 && out_dtype != BWG_OUT_FP16)
     return BWG_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0) return BWG_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return BWG_OK;
   if (D == nullptr || ldd < N) return BWG_ERR_INVALID_ARG;
-  if (K > 0 && (A == nullptr || B == nullptr || lda < K || ldb < N)) return BWG_ERR_INVALID_ARG;
+  if (K > 0 && (A == nullptr || B == nullptr || lda < K || ldb < (b_kmajor ? K : N)))
+    return BWG_ERR_INVALID_ARG;
   if (!aligned16(D) || (static_cast<long long>(ldd) * out_elt(out_dtype)) % 16 != 0)
     return BWG_ERR_ALIGNMENT;
   if (K > 0 && (!aligned16(A) || !aligned16(B) || (static_cast<long long>(lda) * 2) % 16 != 0 ||
@@ -588,8 +591,9 @@ bwg_status launch_status(cudaError_t e) {
 }
 
 bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M, int N, int K,
-                     int lda, int ldb, int ldd, int out_dtype, cudaStream_t stream) {
-  bwg_status s = check_args(A, B, D, M, N, K, lda, ldb, ldd, out_dtype);
+                     int lda, int ldb, int ldd, int out_dtype, cudaStream_t stream,
+                     bool b_kmajor = false) {
+  bwg_status s = check_args(A, B, D, M, N, K, lda, ldb, ldd, out_dtype, b_kmajor);
   if (s != BWG_OK) return s;
   if (M == 0 || N == 0) return BWG_OK;
   DeviceState* st = nullptr;
@@ -597,7 +601,7 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
   bwg_plan_info pl;
   s = plan_dense(M, N, K, out_dtype, fp16_in, st->sm_count, st->max_smem, force_kernel_from_env(),
                  force_stages_from_env(), st->clusters_2cta, st->ctas_1cta, st->clusters_mc,
-                 st->clusters_2c, &pl, st->clusters_small);
+                 st->clusters_2c, &pl, st->clusters_small, false, b_kmajor);
   if (s != BWG_OK) return s;
   if (pl.kernel == BWG_KERNEL_ZERO)
     return launch_status(launch_zero_fill(D, M, N, ldd, out_elt(out_dtype), stream));
@@ -608,8 +612,8 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
     SmallMParams p;
     std::memset(&p, 0, sizeof(p));
     const int m_pad = pl.mma_n;
-    if (!get_map(&p.map_bt, B, in_t, N, K, static_cast<uint64_t>(ldb) * 2, 64, kBK,
-                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!get_map(&p.map_bt, B, in_t, b_kmajor ? K : N, b_kmajor ? N : K, static_cast<uint64_t>(ldb) * 2,
+                 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !get_map(&p.map_at, A, in_t, K, M, static_cast<uint64_t>(lda) * 2, kBK, m_pad,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
         !get_map(&p.map_d, D, out_map_dtype(out_dtype), N, M, static_cast<uint64_t>(ldd) * oe,
@@ -634,6 +638,7 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
     p.tx_extra = g_tx_extra.load();
     p.streamk = pl.streamk;
     p.split = pl.split;
+    p.b_kmajor = b_kmajor ? 1 : 0;
     p.staging_in_ring = pl.staging_in_ring;
     p.d = D;
     p.ldd = ldd;
@@ -653,8 +658,8 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
   const uint32_t d_box_inner = out_dtype == BWG_OUT_FP32 ? 32 : 64;
   if (!get_map(&p.map_a, A, in_t, K, M, static_cast<uint64_t>(lda) * 2, kBK, kRowsPerCta,
                CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !get_map(&p.map_b, B, in_t, N, K, static_cast<uint64_t>(ldb) * 2, 64, kBK,
-               CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !get_map(&p.map_b, B, in_t, b_kmajor ? K : N, b_kmajor ? N : K, static_cast<uint64_t>(ldb) * 2,
+               64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !get_map(&p.map_d, D, out_map_dtype(out_dtype), N, M, static_cast<uint64_t>(ldd) * oe,
                d_box_inner, 32, CU_TENSOR_MAP_SWIZZLE_128B))
     return BWG_ERR_CUDA;
@@ -665,6 +670,7 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
   p.N = N;
   p.K = K;
   p.ldd = ldd;
+  p.b_kmajor = b_kmajor ? 1 : 0;
   p.num_m_tiles = ceil_div(M, pl.tile_m);
   p.num_n_tiles = ceil_div(N, pl.tile_n);
   p.num_k_blocks = pl.k_blocks;
@@ -701,9 +707,10 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
 // N/2] = silu(gate) * up.  The up block starts at column N/2, which a TMA
 // load's first coordinate must reach on a 16-byte boundary: N/2 a multiple
 // of 8, i.e. N a multiple of 16.
+// b_kmajor: each B[g] is stored [N, K] (the pages' layout) instead of [K, N].
 bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
                        const int* group_offsets, int G, int M_total, int N, int K,
-                       cudaStream_t stream, bool swiglu = false) {
+                       cudaStream_t stream, bool swiglu = false, bool b_kmajor = false) {
   if (G < 0 || M_total < 0 || N < 0 || K < 0) return BWG_ERR_INVALID_ARG;
   if (G == 0 || M_total == 0 || N == 0) return BWG_OK;
   if (D == nullptr || group_offsets == nullptr) return BWG_ERR_INVALID_ARG;
@@ -744,7 +751,8 @@ bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
                  n_out, M_total, static_cast<uint64_t>(n_out) * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
       return BWG_ERR_CUDA;
     for (int i = 0; i < gn; ++i)
-      if (!get_map(&P.map_b[i], B[g0 + i], in_t, N, K, static_cast<uint64_t>(N) * 2, 64, kBK,
+      if (!get_map(&P.map_b[i], B[g0 + i], in_t, b_kmajor ? K : N, b_kmajor ? N : K,
+                   static_cast<uint64_t>(b_kmajor ? K : N) * 2, 64, 64,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return BWG_ERR_CUDA;
     p.err = st->err;
@@ -762,7 +770,8 @@ bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
     p.group_m = kGroupM;
     p.stages = stages;
     p.out_dtype = fp16 ? BWG_OUT_FP16 : BWG_OUT_BF16;
-    p.idesc = make_idesc_f16(fp16 ? kFmtF16 : kFmtBF16, false, true, 2 * kRowsPerCta, kTileN);
+    p.idesc = make_idesc_f16(fp16 ? kFmtF16 : kFmtBF16, false, !b_kmajor, 2 * kRowsPerCta, kTileN);
+    p.b_kmajor = b_kmajor ? 1 : 0;
     p.tx_extra = g_tx_extra.load();
     p.trace = g_trace.load();
     p.G = gn;
@@ -775,7 +784,7 @@ bwg_status run_grouped(bool fp16, const void* A, const void* const* B, void* D,
       // tiles here are bound by how fast shared memory fills, so it measured
       // no faster than the padded tile.  BWG_GROUPED_SWAP=1 turns it on.
       const char* v = std::getenv("BWG_GROUPED_SWAP");
-      p.swap_ends = (v != nullptr && v[0] == '1' && !swiglu) ? 1 : 0;
+      p.swap_ends = (v != nullptr && v[0] == '1' && !swiglu && !b_kmajor) ? 1 : 0;
     }
     // Upper bound on tiles: every group adds at most one partial row tile.
     const long long max_tiles =
@@ -958,6 +967,46 @@ bwg_status grouped_gemm_swiglu_fp16(const void* A, const void* const* B, void* H
                                     void* stream) {
   return run_grouped(true, A, B, H, group_offsets, G, M_total, N, K,
                      static_cast<cudaStream_t>(stream), true);
+}
+
+bwg_status gemm_bf16_nt(const void* A, const void* B, void* D, int M, int N, int K, int lda, int ldb,
+                        int ldd, int out_dtype, void* stream) {
+  return run_dense(false, A, B, D, M, N, K, lda, ldb, ldd, out_dtype,
+                   static_cast<cudaStream_t>(stream), /*b_kmajor=*/true);
+}
+
+bwg_status gemm_fp16_nt(const void* A, const void* B, void* D, int M, int N, int K, int lda, int ldb,
+                        int ldd, int out_dtype, void* stream) {
+  return run_dense(true, A, B, D, M, N, K, lda, ldb, ldd, out_dtype,
+                   static_cast<cudaStream_t>(stream), /*b_kmajor=*/true);
+}
+
+bwg_status grouped_gemm_bf16_nt(const void* A, const void* const* B, void* D,
+                                const int* group_offsets, int G, int M_total, int N, int K,
+                                void* stream) {
+  return run_grouped(false, A, B, D, group_offsets, G, M_total, N, K,
+                     static_cast<cudaStream_t>(stream), false, /*b_kmajor=*/true);
+}
+
+bwg_status grouped_gemm_fp16_nt(const void* A, const void* const* B, void* D,
+                                const int* group_offsets, int G, int M_total, int N, int K,
+                                void* stream) {
+  return run_grouped(true, A, B, D, group_offsets, G, M_total, N, K,
+                     static_cast<cudaStream_t>(stream), false, /*b_kmajor=*/true);
+}
+
+bwg_status grouped_gemm_swiglu_bf16_nt(const void* A, const void* const* B, void* H,
+                                       const int* group_offsets, int G, int M_total, int N, int K,
+                                       void* stream) {
+  return run_grouped(false, A, B, H, group_offsets, G, M_total, N, K,
+                     static_cast<cudaStream_t>(stream), true, /*b_kmajor=*/true);
+}
+
+bwg_status grouped_gemm_swiglu_fp16_nt(const void* A, const void* const* B, void* H,
+                                       const int* group_offsets, int G, int M_total, int N, int K,
+                                       void* stream) {
+  return run_grouped(true, A, B, H, group_offsets, G, M_total, N, K,
+                     static_cast<cudaStream_t>(stream), true, /*b_kmajor=*/true);
 }
 
 bwg_status gemm_bf16_small_m_noalloc(const void* A, const void* B, void* D, int M, int N, int K,

@@ -197,8 +197,15 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
         const int k0 = kb * kBK;
         const uint32_t sbt = smem_bt + s * kBtStageBytes;
         mbar_arrive_expect_tx(full, tx);
-        tma_load_2d(sbt, &p.map_bt, full, n0, k0);
-        tma_load_2d(sbt + kBtChunkBytes, &p.map_bt, full, n0 + 64, k0);
+        // B^T's 128 channels x 64 K as two 64-channel boxes: row-major B
+        // [K, N] is addressed (channel, k), B stored as [N, K] (k, channel)
+        if (p.b_kmajor) {
+          tma_load_2d(sbt, &p.map_bt, full, k0, n0);
+          tma_load_2d(sbt + kBtChunkBytes, &p.map_bt, full, k0, n0 + 64);
+        } else {
+          tma_load_2d(sbt, &p.map_bt, full, n0, k0);
+          tma_load_2d(sbt + kBtChunkBytes, &p.map_bt, full, n0 + 64, k0);
+        }
         tma_load_2d(smem_at + s * at_stage_bytes, &p.map_at, full, k0, 0);
         if (++s == S) {
           s = 0;
@@ -251,12 +258,15 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
           tc_fence_after();
           // MMA A = B^T tile (MN-major, two 64-channel boxes 8 KiB apart),
           // MMA B = A tile (K-major, 128-byte rows, 8-row groups 1 KiB apart).
-          const uint64_t a_desc =
-              make_smem_desc(smem_bt + s * kBtStageBytes, kBtChunkBytes, 1024, kSwizzle128B);
+          // (B stored as [N, K]: the MMA A operand is K-major, 8-row groups
+          // 1 KiB apart, the next 16 K values 32 bytes along each row.)
+          const uint64_t a_desc = make_smem_desc(smem_bt + s * kBtStageBytes,
+                                                 p.b_kmajor ? 16u : kBtChunkBytes, 1024, kSwizzle128B);
+          const uint32_t a_step = p.b_kmajor ? 32u : 2048u;
           const uint64_t b_desc = make_smem_desc(smem_at + s * at_stage_bytes, 16, 1024, kSwizzle128B);
 #pragma unroll
           for (uint32_t kk = 0; kk < kBK / 16; ++kk)
-            mma_f16<1>(d_tmem, a_desc + ((kk * 2048u) >> 4), b_desc + ((kk * 32u) >> 4), p.idesc,
+            mma_f16<1>(d_tmem, a_desc + ((kk * a_step) >> 4), b_desc + ((kk * 32u) >> 4), p.idesc,
                        (kb > kb0 || kk > 0) ? 1u : 0u);
           mma_commit_1cta(empty_bar(s));
           if (++s == S) {

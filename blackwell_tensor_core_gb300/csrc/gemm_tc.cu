@@ -438,6 +438,10 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
         const int b_col = SW ? tl.n0 + static_cast<int>(rank) * p.swiglu_up
                              : tl.n0 + static_cast<int>(rank * b_cols);
         const CUtensorMap* mb = b_map<CG, GROUPED>(P, tl.g);
+        // B box j: 64 columns of D x 64 K.  Row-major B [K, N] (MN-major
+        // operand) is addressed (column, k); B stored as [N, K] (K-major, the
+        // layout of the pages' kernels) is addressed (k, column).
+        const bool bk = p.b_kmajor != 0;
         for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, p.timeout_ns)) {
             record_fault(p.err, kFaultTimeout, kRoleProducer, kBarEmpty, s, ph ^ 1u);
@@ -455,21 +459,27 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
               if ((tl.cmask >> c) & 1)
                 tma_load_2d_pair(sa + c * kAStageBytes, &p.map_a, fb, k0, a_row + c * 2 * kRowsPerCta);
             if constexpr (MC == 1) {
-              for (uint32_t j = 0; j < b_chunks; ++j)
-                tma_load_2d_pair(sb + j * kBChunkBytes, mb, fb, b_col + 64 * j, k0);
+              for (uint32_t j = 0; j < b_chunks; ++j) {
+                const int c = b_col + 64 * static_cast<int>(j);
+                tma_load_2d_pair(sb + j * kBChunkBytes, mb, fb, bk ? k0 : c, bk ? c : k0);
+              }
             } else {
               // The pairs share B: box j of this CTA's columns is fetched once, by
               // pair j, and multicast to the same-rank CTA of every pair; each
               // destination's bytes complete on its own pair leader's barrier.
               const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (rank + 2)));
-              for (uint32_t j = pair; j < b_chunks; j += MC)
-                tma_load_2d_pair_mc(sb + j * kBChunkBytes, mb, fb, b_col + 64 * j, k0, mask);
+              for (uint32_t j = pair; j < b_chunks; j += MC) {
+                const int c = b_col + 64 * static_cast<int>(j);
+                tma_load_2d_pair_mc(sb + j * kBChunkBytes, mb, fb, bk ? k0 : c, bk ? c : k0, mask);
+              }
             }
           } else {
             mbar_arrive_expect_tx(full_bar(s), stage_tx);
             tma_load_2d(sa, &p.map_a, full_bar(s), k0, a_row);
-            for (uint32_t j = 0; j < b_chunks; ++j)
-              tma_load_2d(sb + j * kBChunkBytes, mb, full_bar(s), b_col + 64 * j, k0);
+            for (uint32_t j = 0; j < b_chunks; ++j) {
+              const int c = b_col + 64 * static_cast<int>(j);
+              tma_load_2d(sb + j * kBChunkBytes, mb, full_bar(s), bk ? k0 : c, bk ? c : k0);
+            }
           }
           if (++s == S) {
             s = 0;
@@ -545,14 +555,19 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
           tc_fence_after();
           const uint64_t a_desc =
               make_smem_desc(smem_a + s * kAStage + cons * kAStageBytes, 16, 1024, kSwizzle128B);
-          const uint64_t b_desc =
-              make_smem_desc(smem_b + s * kBStageBytes, kBChunkBytes, 1024, kSwizzle128B);
+          // MN-major B: 64-column chunks 8 KiB apart (LBO), the next 16 K
+          // values 16 rows (2048 bytes) further.  K-major B: 8-row groups 1 KiB
+          // apart, the next 16 K values 32 bytes along each row, as for A.
+          const bool bk = p.b_kmajor != 0;
+          const uint64_t b_desc = make_smem_desc(smem_b + s * kBStageBytes, bk ? 16u : kBChunkBytes,
+                                                 1024, kSwizzle128B);
+          const uint32_t b_step = bk ? 32u : 2048u;
 #pragma unroll
           for (uint32_t kk = 0; kk < kBK / 16; ++kk) {
             // K-major A: the next 16 K values are 32 bytes further along each
-            // 128-byte row.  MN-major B: they are 16 rows (2048 bytes) further.
+            // 128-byte row.
             const uint64_t ad = a_desc + ((kk * 32u) >> 4);
-            const uint64_t bd = b_desc + ((kk * 2048u) >> 4);
+            const uint64_t bd = b_desc + ((kk * b_step) >> 4);
             mma_f16<CG>(d_tmem, swapped ? bd : ad, swapped ? ad : bd, idesc,
                         (kb != tl.kb0 || kk != 0) ? 1u : 0u);
           }

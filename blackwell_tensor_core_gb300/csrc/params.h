@@ -35,7 +35,8 @@ constexpr unsigned long long kFaultBadOffsets = 2;
 
 struct GemmParams {
   CUtensorMap map_a;  // A [rows, K] bf16/fp16, box {64 (K), 128 (rows)}, 128B swizzle
-  CUtensorMap map_b;  // B [K, N], box {64 (N), 64 (K)}, 128B swizzle (dense only)
+  CUtensorMap map_b;  // B [K, N], box {64 (N), 64 (K)}; or B [N, K] (b_kmajor), box {64 (K), 64 (N)};
+                      // 128B swizzle (dense only)
   CUtensorMap map_d;  // D [rows, N], box {64 or 32 (N), 32 (rows)}, 128B swizzle
   unsigned long long* err;
   void* d_ptr;               // D base, for masked row stores at ragged group ends
@@ -54,6 +55,7 @@ struct GemmParams {
   int swap_ends;             // grouped: 1 = compute group ends of <= 128 rows with swapped operands
   uint32_t idesc_swap;       // grouped: descriptor of the swapped MMA (A MN-major, B K-major)
   int swiglu_up;             // SwiGLU kernels: first column of the up block in B (= N of H)
+  int b_kmajor;              // 1: B is stored [N, K] (K-major operand), 0: [K, N]
   int workers;               // dynamic scheduling: CTA pairs that run at once (last-wave cut)
   // Stream-K last wave (dense two-consumer kernel, static schedule): the last
   // sk_tiles tiles of the raster order are shared out by k-blocks over all
@@ -78,7 +80,8 @@ struct GroupedParams {
 };
 
 struct SmallMParams {
-  CUtensorMap map_bt;  // B [K, N] viewed as the MMA's MN-major A: box {64 (N), 64 (K)}
+  CUtensorMap map_bt;  // B [K, N] viewed as the MMA's MN-major A: box {64 (N), 64 (K)};
+                       // with b_kmajor, B [N, K] as a K-major A: box {64 (K), 64 (N)}
   CUtensorMap map_at;  // A [M, K] as the MMA's K-major B: box {64 (K), m_pad (rows)}
   CUtensorMap map_d;   // D [M, N], box {min(64, tile_n) (N), m_pad (rows)}, no swizzle
   CUtensorMap map_d2;  // D [M, N], box {tile_n - 64 (N), m_pad}, when tile_n > 64
@@ -98,6 +101,7 @@ struct SmallMParams {
   // tile t, and the cluster sums its partials through distributed shared
   // memory, each CTA finishing ceil(M/split) rows of D, which it stores itself.
   int split;
+  int b_kmajor;         // 1: B is stored [N, K]
   int staging_in_ring;  // 1: one tile per CTA, the output staging tile sits in the idle ring
   void* d;            // D (split mode stores its rows directly)
   long long ldd;      // D's leading dimension, elements

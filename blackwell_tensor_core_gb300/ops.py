@@ -58,12 +58,13 @@ def lib() -> ctypes.CDLL:
                                    "There is no fallback implementation." % LIB_PATH)
             L = ctypes.CDLL(LIB_PATH)
             vp, i, u32, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64
-            for name in ("gemm_bf16", "gemm_fp16"):
+            for name in ("gemm_bf16", "gemm_fp16", "gemm_bf16_nt", "gemm_fp16_nt"):
                 f = getattr(L, name)
                 f.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp]
                 f.restype = i
             for name in ("grouped_gemm_bf16", "grouped_gemm_fp16", "grouped_gemm_swiglu_bf16",
-                         "grouped_gemm_swiglu_fp16"):
+                         "grouped_gemm_swiglu_fp16", "grouped_gemm_bf16_nt", "grouped_gemm_fp16_nt",
+                         "grouped_gemm_swiglu_bf16_nt", "grouped_gemm_swiglu_fp16_nt"):
                 f = getattr(L, name)
                 f.argtypes = [vp, ctypes.POINTER(vp), vp, vp, i, i, i, i, vp]
                 f.restype = i
@@ -153,12 +154,13 @@ def _matrix(t: torch.Tensor, name: str) -> int:
 
 
 def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None,
-         out_dtype: torch.dtype = torch.bfloat16, stream=None) -> torch.Tensor:
-    """D = A @ B through gemm_bf16 / gemm_fp16 (chosen by A's dtype)."""
+         out_dtype: torch.dtype = torch.bfloat16, stream=None, b_transposed: bool = False) -> torch.Tensor:
+    """D = A @ B through gemm_bf16 / gemm_fp16 (chosen by A's dtype); with
+    ``b_transposed`` B is given as [N, K] and D = A @ B.T (gemm_*_nt)."""
     if A.dtype != B.dtype or A.dtype not in (torch.bfloat16, torch.float16):
         raise TypeError("A and B must both be bfloat16 or both float16")
     M, K = A.shape
-    K2, N = B.shape
+    N, K2 = B.shape if b_transposed else (B.shape[1], B.shape[0])
     if K2 != K:
         raise ValueError("inner dimensions differ: %s x %s" % (tuple(A.shape), tuple(B.shape)))
     if out is None:
@@ -166,7 +168,10 @@ def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None,
     if out.dtype not in _OUT_CODES:
         raise TypeError("output dtype must be bfloat16, float16 or float32")
     lda, ldb, ldd = _matrix(A, "A"), _matrix(B, "B"), _matrix(out, "out")
-    fn = gemm_bf16 if A.dtype == torch.bfloat16 else gemm_fp16
+    if b_transposed:
+        fn = gemm_bf16_nt if A.dtype == torch.bfloat16 else gemm_fp16_nt
+    else:
+        fn = gemm_bf16 if A.dtype == torch.bfloat16 else gemm_fp16
     fn(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, lda, ldb, ldd, _OUT_CODES[out.dtype],
        _stream_handle(stream, A.device))
     return out
@@ -182,20 +187,37 @@ def gemm_fp16(A_ptr: int, B_ptr: int, D_ptr: int, M: int, N: int, K: int, lda: i
     _check(lib().gemm_fp16(A_ptr, B_ptr, D_ptr, M, N, K, lda, ldb, ldd, out_dtype, stream), "gemm_fp16")
 
 
+def gemm_bf16_nt(A_ptr: int, B_ptr: int, D_ptr: int, M: int, N: int, K: int, lda: int, ldb: int,
+                 ldd: int, out_dtype: int, stream: int) -> None:
+    """D = A x B^T with B stored [N, K] (ldb >= K)."""
+    _check(lib().gemm_bf16_nt(A_ptr, B_ptr, D_ptr, M, N, K, lda, ldb, ldd, out_dtype, stream),
+           "gemm_bf16_nt")
+
+
+def gemm_fp16_nt(A_ptr: int, B_ptr: int, D_ptr: int, M: int, N: int, K: int, lda: int, ldb: int,
+                 ldd: int, out_dtype: int, stream: int) -> None:
+    _check(lib().gemm_fp16_nt(A_ptr, B_ptr, D_ptr, M, N, K, lda, ldb, ldd, out_dtype, stream),
+           "gemm_fp16_nt")
+
+
 def grouped_gemm(A: torch.Tensor, Bs: list, group_offsets: torch.Tensor,
-                 out: torch.Tensor | None = None, stream=None, swiglu: bool = False) -> torch.Tensor:
+                 out: torch.Tensor | None = None, stream=None, swiglu: bool = False,
+                 b_transposed: bool = False) -> torch.Tensor:
     """Grouped expert product through grouped_gemm_bf16 / grouped_gemm_fp16.
 
     With ``swiglu`` each weight is [gate | up] ([K, N]) and the result is
-    silu(gate) * up, [M_total, N/2], through grouped_gemm_swiglu_bf16/_fp16."""
+    silu(gate) * up, [M_total, N/2], through grouped_gemm_swiglu_bf16/_fp16.
+    With ``b_transposed`` every weight is given as [N, K] (the *_nt entry points)."""
     if A.dtype not in (torch.bfloat16, torch.float16):
         raise TypeError("A must be bfloat16 or float16")
     M_total, K = A.shape
     G = len(Bs)
-    N = Bs[0].shape[1] if G else 0
+    N = (Bs[0].shape[0] if b_transposed else Bs[0].shape[1]) if G else 0
+    want = (N, K) if b_transposed else (K, N)
     for b in Bs:
-        if b.shape != (K, N) or b.dtype != A.dtype or not b.is_contiguous():
-            raise ValueError("every weight matrix must be a contiguous [K, N] tensor of A's dtype")
+        if b.shape != want or b.dtype != A.dtype or not b.is_contiguous():
+            raise ValueError("every weight matrix must be a contiguous %s tensor of A's dtype"
+                             % ("[N, K]" if b_transposed else "[K, N]"))
     if group_offsets.dtype != torch.int32 or group_offsets.numel() != G + 1 or not group_offsets.is_cuda:
         raise ValueError("group_offsets must be a CUDA int32 tensor with G+1 entries")
     if not A.is_contiguous():
@@ -205,10 +227,15 @@ def grouped_gemm(A: torch.Tensor, Bs: list, group_offsets: torch.Tensor,
         out = torch.empty((M_total, n_out), dtype=A.dtype, device=A.device)
     elif out.shape != (M_total, n_out) or out.dtype != A.dtype or not out.is_contiguous():
         raise ValueError("out must be a dense [M_total, %d] tensor of A's dtype" % n_out)
-    if swiglu:
-        fn = grouped_gemm_swiglu_bf16 if A.dtype == torch.bfloat16 else grouped_gemm_swiglu_fp16
+    bf = A.dtype == torch.bfloat16
+    if swiglu and b_transposed:
+        fn = grouped_gemm_swiglu_bf16_nt if bf else grouped_gemm_swiglu_fp16_nt
+    elif swiglu:
+        fn = grouped_gemm_swiglu_bf16 if bf else grouped_gemm_swiglu_fp16
+    elif b_transposed:
+        fn = grouped_gemm_bf16_nt if bf else grouped_gemm_fp16_nt
     else:
-        fn = grouped_gemm_bf16 if A.dtype == torch.bfloat16 else grouped_gemm_fp16
+        fn = grouped_gemm_bf16 if bf else grouped_gemm_fp16
     fn(A.data_ptr(), [b.data_ptr() for b in Bs], out.data_ptr(), group_offsets.data_ptr(), G, M_total,
        N, K, _stream_handle(stream, A.device))
     return out
@@ -297,3 +324,29 @@ def grouped_gemm_swiglu_fp16(A_ptr: int, B_ptrs: list, H_ptr: int, offsets_ptr: 
     _check(lib().grouped_gemm_swiglu_fp16(A_ptr, p, H_ptr, offsets_ptr, G, M_total, N, K, stream),
            "grouped_gemm_swiglu_fp16")
     del keep
+
+
+def _grouped_call(name: str, A_ptr: int, B_ptrs: list, D_ptr: int, offsets_ptr: int, G: int,
+                  M_total: int, N: int, K: int, stream: int) -> None:
+    p, keep = _ptr_array(B_ptrs)
+    _check(getattr(lib(), name)(A_ptr, p, D_ptr, offsets_ptr, G, M_total, N, K, stream), name)
+    del keep
+
+
+def grouped_gemm_bf16_nt(A_ptr, B_ptrs, D_ptr, offsets_ptr, G, M_total, N, K, stream) -> None:
+    """Grouped product with every B[g] stored [N, K]."""
+    _grouped_call("grouped_gemm_bf16_nt", A_ptr, B_ptrs, D_ptr, offsets_ptr, G, M_total, N, K, stream)
+
+
+def grouped_gemm_fp16_nt(A_ptr, B_ptrs, D_ptr, offsets_ptr, G, M_total, N, K, stream) -> None:
+    _grouped_call("grouped_gemm_fp16_nt", A_ptr, B_ptrs, D_ptr, offsets_ptr, G, M_total, N, K, stream)
+
+
+def grouped_gemm_swiglu_bf16_nt(A_ptr, B_ptrs, H_ptr, offsets_ptr, G, M_total, N, K, stream) -> None:
+    _grouped_call("grouped_gemm_swiglu_bf16_nt", A_ptr, B_ptrs, H_ptr, offsets_ptr, G, M_total, N, K,
+                  stream)
+
+
+def grouped_gemm_swiglu_fp16_nt(A_ptr, B_ptrs, H_ptr, offsets_ptr, G, M_total, N, K, stream) -> None:
+    _grouped_call("grouped_gemm_swiglu_fp16_nt", A_ptr, B_ptrs, H_ptr, offsets_ptr, G, M_total, N, K,
+                  stream)

@@ -122,6 +122,33 @@ bwg_status grouped_gemm_swiglu_fp16(const void* A, const void* const* B, void* H
                                     void* stream);
 
 /*
+ * The same products with B stored transposed, as B[N, K] row-major (ldb >= K):
+ *   D[M,N] = A[M,K] x B^T.  This is the layout of the pages' own kernels
+ * ("使用 Warp Specialization 和 Cluster 扩展 GEMM" keeps B as (N, K)) and of
+ * weights stored [out_features, in_features].  B then enters the tensor cores
+ * as a K-major operand, like A; every kernel, tile and schedule of the
+ * [K, N] form applies, with the same rules, statuses and results.  For the
+ * grouped forms each B[g] is [N, K] with leading dimension K; with SwiGLU,
+ * rows 0 .. N/2-1 of B[g] are the gate block and rows N/2 .. N-1 the up block.
+ */
+bwg_status gemm_bf16_nt(const void* A, const void* B, void* D, int M, int N, int K, int lda, int ldb,
+                        int ldd, int out_dtype, void* stream);
+bwg_status gemm_fp16_nt(const void* A, const void* B, void* D, int M, int N, int K, int lda, int ldb,
+                        int ldd, int out_dtype, void* stream);
+bwg_status grouped_gemm_bf16_nt(const void* A, const void* const* B, void* D,
+                                const int* group_offsets, int G, int M_total, int N, int K,
+                                void* stream);
+bwg_status grouped_gemm_fp16_nt(const void* A, const void* const* B, void* D,
+                                const int* group_offsets, int G, int M_total, int N, int K,
+                                void* stream);
+bwg_status grouped_gemm_swiglu_bf16_nt(const void* A, const void* const* B, void* H,
+                                       const int* group_offsets, int G, int M_total, int N, int K,
+                                       void* stream);
+bwg_status grouped_gemm_swiglu_fp16_nt(const void* A, const void* const* B, void* H,
+                                       const int* group_offsets, int G, int M_total, int N, int K,
+                                       void* stream);
+
+/*
  * No-allocation form of gemm_bf16 for small M (M <= 128).  The pages have no
  * counterpart: it exists for callers that cannot let the library call
  * cudaMalloc -- programs that hand all device memory to their own pool
