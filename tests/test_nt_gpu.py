@@ -118,12 +118,18 @@ def test_nt_bad_leading_dimension():
     assert st == 2  # ldb * 2 not a multiple of 16 bytes
 
 
-@pytest.mark.parametrize("swiglu", [False, True])
-def test_grouped_nt_exact_and_matches_row_major(swiglu):
+@pytest.mark.parametrize("swiglu,one_consumer,sched", [(False, False, "clc"), (True, False, "clc"),
+                                                       (False, True, "static"), (True, True, "static"),
+                                                       (False, False, "static")])
+def test_grouped_nt_exact_and_matches_row_major(swiglu, one_consumer, sched, monkeypatch):
     """Grouped expert product with weights stored [N, K] (plain and SwiGLU,
-    empty and ragged groups): exact on integer inputs, and the same results as
-    the [K, N] entry point on the transposed weights."""
+    both grouped kernels and both schedulers, empty and ragged groups): exact
+    on integer inputs, and the same results as the [K, N] entry point on the
+    transposed weights."""
     from blackwell_tensor_core_gb300 import ops
+    monkeypatch.setenv("BWG_SCHED", sched)
+    if one_consumer:
+        monkeypatch.setenv("BWG_GROUPED_1C", "1")
     counts = [300, 0, 513, 7, 256]
     off = wl.offsets_from_counts(counts)
     g = wl.generator(9300 + int(swiglu))
