@@ -260,15 +260,21 @@ def oracle_rows_tflops(A_bits, B_bits, rows, start_row=0):
 
 
 def cpu_baseline(case, budget_s=12.0):
-    """The oracle as it stands on a bounded row sample of the same product."""
+    """The oracle as it stands on a bounded row sample of the same product:
+    blocks of rows, in order, until about `budget_s` seconds of work."""
     import oracle
     from blackwell_tensor_core_gb300 import workloads as wl
     oracle.build()
     Ab, Bb = wl.bits(case.A), wl.bits(case.B)
-    probe = 4
-    _, dt = oracle_rows_tflops(Ab, Bb, probe)
-    rows = int(max(probe, min(case.M, budget_s / max(dt / probe, 1e-9))))
-    val, dt = oracle_rows_tflops(Ab, Bb, rows, probe)
+    oracle_rows_tflops(Ab, Bb, 4)  # load the library, touch the inputs
+    rows, dt, start = 0, 0.0, 0
+    block = 2 * oracle.num_threads()
+    while dt < budget_s and start + block <= case.M:
+        _, t = oracle_rows_tflops(Ab, Bb, block, start)
+        rows += block
+        dt += t
+        start += block
+    val = 2.0 * rows * case.N * case.K / dt / 1e12
     return {"value": val, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": "%d rows of the %dx%dx%d product (%d outputs, K=%d), FP64, %.1f s"
                       % (rows, case.M, case.N, case.K, rows * case.N, case.K, dt)}
