@@ -77,9 +77,9 @@ EncodeTiledFn g_encode = nullptr;
 
 struct MapKey {
   const void* ptr;
-  uint64_t inner, outer, row_bytes;
-  uint32_t box_inner, box_outer;
-  int dtype, swizzle, device;
+  uint64_t dims[4], strides[3];
+  uint32_t box[4];
+  int rank, dtype, swizzle, device;
   bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
 };
 struct MapKeyHash {
@@ -201,6 +201,16 @@ int small_m_smem(int m_pad, int out_dtype, int stages, bool staging_in_ring = fa
 }
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Whether the small-M kernel fills its ring two stages per load: the views
+// that take two k-blocks (and, for row-major B, both channel halves) at once
+// tile the matrices exactly only when K (and N) are multiples of 64.
+// BWG_SMALL_M_PAIRS=0 turns it off.
+bool small_m_pairs_ok(int N, int K, int stages, bool b_kmajor) {
+  const char* v = std::getenv("BWG_SMALL_M_PAIRS");
+  if (v != nullptr && v[0] == '0') return false;
+  return K % 64 == 0 && stages >= 2 && (b_kmajor || N % 64 == 0);
+}
 
 int group_m_from_env() {
   const char* v = std::getenv("BWG_GROUP_M");
@@ -335,6 +345,8 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     o->smem_input_per_cta = stages * small_m_stage_bytes(m_pad);
     o->smem_total = small_m_smem(m_pad, out_dtype, stages, in_ring);
     o->staging_in_ring = in_ring ? 1 : 0;
+    o->bt_loads = (b_kmajor || N % 64 == 0) ? 1 : 2;
+    o->pair_loads = small_m_pairs_ok(N, K, stages, b_kmajor) ? 1 : 0;
     // each CTA's partial and the rows it receives fit in its idle stage ring
     if (split > 1 && (static_cast<long long>(m_pad) + static_cast<long long>(split) * ceil_div(M, split)) * 512 >
                          static_cast<long long>(stages) * small_m_stage_bytes(m_pad))
@@ -525,19 +537,23 @@ bwg_status ensure_device(DeviceState** out) {
   return st.init_status;
 }
 
-bool get_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dtype, uint64_t inner,
-             uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-             CUtensorMapSwizzle swizzle) {
+// Tensor map of a rank-`rank` view (2 to 4 dimensions, innermost first;
+// strides in bytes for dimensions 1.., box in elements), cached by its
+// arguments.
+bool get_map_nd(CUtensorMap* m, const void* ptr, CUtensorMapDataType dtype, int rank,
+                const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                CUtensorMapSwizzle swizzle) {
   int dev = 0;
   cudaGetDevice(&dev);
   MapKey key;
   std::memset(&key, 0, sizeof(key));
   key.ptr = ptr;
-  key.inner = inner;
-  key.outer = outer;
-  key.row_bytes = row_bytes;
-  key.box_inner = box_inner;
-  key.box_outer = box_outer;
+  for (int d = 0; d < rank; ++d) {
+    key.dims[d] = dims[d];
+    key.box[d] = box[d];
+    if (d + 1 < rank) key.strides[d] = strides[d];
+  }
+  key.rank = rank;
   key.dtype = static_cast<int>(dtype);
   key.swizzle = static_cast<int>(swizzle);
   key.device = dev;
@@ -547,18 +563,81 @@ bool get_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dtype, uint64_
     *m = it->second;
     return true;
   }
-  cuuint64_t gdim[2] = {inner, outer};
-  cuuint64_t gstride[1] = {row_bytes};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estride[2] = {1, 1};
+  cuuint64_t gdim[4], gstride[3];
+  cuuint32_t bx[4], estride[4] = {1, 1, 1, 1};
+  for (int d = 0; d < rank; ++d) {
+    gdim[d] = dims[d];
+    bx[d] = box[d];
+    if (d + 1 < rank) gstride[d] = strides[d];
+  }
   CUtensorMap map;
-  if (g_encode(&map, dtype, 2, const_cast<void*>(ptr), gdim, gstride, box, estride,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  if (g_encode(&map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), gdim, gstride, bx,
+               estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
   if (g_maps.size() > 8192) g_maps.clear();
   g_maps.emplace(key, map);
   *m = map;
+  return true;
+}
+
+// 2-D map of a row-major matrix: `inner` elements per row, `outer` rows,
+// `row_bytes` apart.
+bool get_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dtype, uint64_t inner,
+             uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+             CUtensorMapSwizzle swizzle) {
+  const uint64_t dims[2] = {inner, outer};
+  const uint32_t box[2] = {box_inner, box_outer};
+  return get_map_nd(m, ptr, dtype, 2, dims, &row_bytes, box, swizzle);
+}
+
+// B^T maps of the small-M kernel (single stage and, where the layout
+// allows, two stages per load) and the two-stage map of A; sets bt_boxes and
+// pair_loads.  Row-major B with N not a multiple of 64 is loaded as two
+// 64-channel boxes a stage.
+bool small_m_operand_maps(SmallMParams* p, const void* A, const void* B, CUtensorMapDataType in_t,
+                          int M, int N, int K, long long lda, long long ldb, int m_pad, int stages,
+                          bool b_kmajor) {
+  const uint64_t bs = static_cast<uint64_t>(ldb) * 2;
+  const uint64_t as = static_cast<uint64_t>(lda) * 2;
+  const bool pairs = small_m_pairs_ok(N, K, stages, b_kmajor);
+  if (b_kmajor) {
+    // B [N, K]: one box of 128 rows (channels) x 64 K a stage
+    if (!get_map(&p->map_bt, B, in_t, K, N, bs, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
+    p->bt_boxes = 1;
+  } else if (N % 64 == 0) {
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(K), static_cast<uint64_t>(N / 64)};
+    const uint64_t strides[2] = {bs, 128};
+    const uint32_t box[3] = {64, 64, 2};
+    if (!get_map_nd(&p->map_bt, B, in_t, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+    p->bt_boxes = 1;
+  } else {
+    if (!get_map(&p->map_bt, B, in_t, N, K, bs, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
+    p->bt_boxes = 2;
+  }
+  p->pair_loads = 0;
+  if (!pairs) return true;
+  const uint64_t kb = static_cast<uint64_t>(K / 64);
+  if (b_kmajor) {
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(N), kb};
+    const uint64_t strides[2] = {bs, 128};
+    const uint32_t box[3] = {64, 128, 2};
+    if (!get_map_nd(&p->map_bt2, B, in_t, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+  } else {
+    const uint64_t dims[4] = {64, 64, static_cast<uint64_t>(N / 64), kb};
+    const uint64_t strides[3] = {bs, 128, 64 * bs};
+    const uint32_t box[4] = {64, 64, 2, 2};
+    if (!get_map_nd(&p->map_bt2, B, in_t, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+  }
+  const uint64_t adims[3] = {64, static_cast<uint64_t>(M), kb};
+  const uint64_t astrides[2] = {as, 128};
+  const uint32_t abox[3] = {64, static_cast<uint32_t>(m_pad), 2};
+  if (!get_map_nd(&p->map_at2, A, in_t, 3, adims, astrides, abox, CU_TENSOR_MAP_SWIZZLE_128B))
+    return false;
+  p->pair_loads = 1;
   return true;
 }
 
@@ -612,8 +691,7 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
     SmallMParams p;
     std::memset(&p, 0, sizeof(p));
     const int m_pad = pl.mma_n;
-    if (!get_map(&p.map_bt, B, in_t, b_kmajor ? K : N, b_kmajor ? N : K, static_cast<uint64_t>(ldb) * 2,
-                 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!small_m_operand_maps(&p, A, B, in_t, M, N, K, lda, ldb, m_pad, pl.stages, b_kmajor) ||
         !get_map(&p.map_at, A, in_t, K, M, static_cast<uint64_t>(lda) * 2, kBK, m_pad,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
         !get_map(&p.map_d, D, out_map_dtype(out_dtype), N, M, static_cast<uint64_t>(ldd) * oe,
@@ -896,6 +974,7 @@ bwg_status run_small_m_noalloc(const void* A, const void* B, void* D, int M, int
   const int oe = out_elt(out_dtype);
   SmallMParams p;
   std::memset(&p, 0, sizeof(p));
+  p.bt_boxes = 2;  // two 2-D boxes a stage, one stage a load
   if (!encode_map_direct(&p.map_bt, B, in_t, N, K, static_cast<uint64_t>(ldb) * 2, 64, kBK,
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_map_direct(&p.map_at, A, in_t, K, M, static_cast<uint64_t>(lda) * 2, kBK, m_pad,

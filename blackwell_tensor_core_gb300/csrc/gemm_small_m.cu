@@ -9,9 +9,14 @@
 // sets at run time in steps of 16, so the tensor cores skip most padding.
 //
 // Operands as stored: B is row-major [K,N], so B^T's 128 channel values for one
-// k are contiguous: the MMA's A operand is MN-major, loaded as 64x64 boxes with
-// 128-byte swizzle.  A is row-major [M,K]: the MMA's B operand is K-major, one
-// box of m_pad rows x 64 K.  The accumulator has TMEM lane = output column and
+// k are contiguous: the MMA's A operand is MN-major, two 64-channel x 64-K
+// blocks with 128-byte swizzle, taken by one load through a 3-D view of B
+// (64 channels, k, channel group).  A is row-major [M,K]: the MMA's B operand
+// is K-major, one box of m_pad rows x 64 K.  Each TMA load has a fixed cost
+// on the SM besides its bytes, and measured on GB300 this kernel streams B at
+// a rate set by the loads per byte: two 64x64 boxes a stage ran 8% slower
+// than one 3-D load, and filling two stages per load (4-D view of B, 3-D of
+// A) gained 8% more.  The accumulator has TMEM lane = output column and
 // TMEM column = row of D, so each epilogue thread owns one output column and
 // writes it down the rows of a [m_pad x 64] staging tile, which a TMA store
 // then writes to D (rows >= M are clipped by the tensor bounds).  No transpose
@@ -155,6 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
     fence_mbarrier_init();
     prefetch_tensormap(&p.map_bt);
     prefetch_tensormap(&p.map_at);
+    if (p.pair_loads) {
+      prefetch_tensormap(&p.map_bt2);
+      prefetch_tensormap(&p.map_at2);
+    }
     prefetch_tensormap(&p.map_d);
     if (p.tile_n > 64) prefetch_tensormap(&p.map_d2);
   }
@@ -164,6 +173,15 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
   // k-block.  It is the thread that initialised the barriers, so it fills
   // the first ring stages before the block-wide barrier below: the first
   // loads are in flight while TMEM is being allocated.
+  //
+  // Each TMA load costs the SM a fixed amount of time besides its bytes:
+  // this kernel streams B at a rate set by how many loads it issues per
+  // byte, not by the bytes alone.  So a stage of B^T is one load where the
+  // layout allows it, and with pair_loads two stages are filled by one load
+  // of B^T and one of A.  The pair completes on the first stage's barrier;
+  // the second stage's barrier gets a plain arrival.  The MMA issuer takes
+  // the stages in order, so it has waited for the pair's bytes before it
+  // reads the second stage.
   struct Producer {
     const SmallMParams& p;
     const Segments& segs;
@@ -189,24 +207,49 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
           continue;
         }
         const uint32_t full = bar0 + 8u * s, empty = bar0 + 8u * (S + s);
-        if (!mbar_wait(empty, ph ^ 1u, p.timeout_ns)) {
-          record_fault_small(p.err, 0, 1, s, ph ^ 1u);
+        const bool pair = p.pair_loads && (s & 1) == 0 && s + 1 < S && kb + 2 <= kb1;
+        bool ok = mbar_wait(empty, ph ^ 1u, p.timeout_ns);
+        if (!ok) record_fault_small(p.err, 0, 1, s, ph ^ 1u);
+        if (ok && pair) {
+          ok = mbar_wait(empty + 8u, ph ^ 1u, p.timeout_ns);
+          if (!ok) record_fault_small(p.err, 0, 1, s + 1, ph ^ 1u);
+        }
+        if (!ok) {
           *aborted = true;
           break;
         }
         const int k0 = kb * kBK;
         const uint32_t sbt = smem_bt + s * kBtStageBytes;
+        const uint32_t sat = smem_at + s * at_stage_bytes;
+        if (pair) {
+          mbar_arrive_expect_tx(full, 2u * (tx - p.tx_extra) + p.tx_extra);
+          if (p.b_kmajor)
+            tma_load_3d(sbt, &p.map_bt2, full, 0, n0, kb);
+          else
+            tma_load_4d(sbt, &p.map_bt2, full, 0, 0, n0 >> 6, kb);
+          tma_load_3d(sat, &p.map_at2, full, 0, 0, kb);
+          mbar_arrive_local(full + 8u);
+          if ((s += 2) == S) {
+            s = 0;
+            ph ^= 1u;
+          }
+          kb += 2;
+          n += 2;
+          continue;
+        }
         mbar_arrive_expect_tx(full, tx);
-        // B^T's 128 channels x 64 K as two 64-channel boxes: row-major B
-        // [K, N] is addressed (channel, k), B stored as [N, K] (k, channel)
+        // B^T's 128 channels x 64 K: row-major B [K, N] is addressed
+        // (channel, k) or (channel in group, k, group), B stored as [N, K]
+        // (k, channel)
         if (p.b_kmajor) {
           tma_load_2d(sbt, &p.map_bt, full, k0, n0);
-          tma_load_2d(sbt + kBtChunkBytes, &p.map_bt, full, k0, n0 + 64);
+        } else if (p.bt_boxes == 1) {
+          tma_load_3d(sbt, &p.map_bt, full, 0, k0, n0 >> 6);
         } else {
           tma_load_2d(sbt, &p.map_bt, full, n0, k0);
           tma_load_2d(sbt + kBtChunkBytes, &p.map_bt, full, n0 + 64, k0);
         }
-        tma_load_2d(smem_at + s * at_stage_bytes, &p.map_at, full, k0, 0);
+        tma_load_2d(sat, &p.map_at, full, k0, 0);
         if (++s == S) {
           s = 0;
           ph ^= 1u;

@@ -80,9 +80,22 @@ struct GroupedParams {
 };
 
 struct SmallMParams {
-  CUtensorMap map_bt;  // B [K, N] viewed as the MMA's MN-major A: box {64 (N), 64 (K)};
-                       // with b_kmajor, B [N, K] as a K-major A: box {64 (K), 64 (N)}
+  // One ring stage of B^T (the MMA's A operand, 128 channels x 64 K):
+  //  - row-major B [K, N], bt_boxes == 1: a 3-D view {64 channels, K, N/64
+  //    channel groups} (strides ldb*2 and 128 bytes), box {64, 64, 2}: both
+  //    64-channel halves of the stage in one load;
+  //  - row-major B, bt_boxes == 2 (N not a multiple of 64): 2-D {N, K}, box
+  //    {64, 64}, one load per half;
+  //  - B stored [N, K] (b_kmajor): 2-D {K, N}, box {64 (K), 128 (rows)}.
+  CUtensorMap map_bt;
   CUtensorMap map_at;  // A [M, K] as the MMA's K-major B: box {64 (K), m_pad (rows)}
+  // Two consecutive ring stages in one load each (pair_loads): B^T as a 4-D
+  // view {64, 64, N/64, K/64} with box {64, 64, 2, 2} (row-major B) or a 3-D
+  // view {64 (K), N, K/64} with box {64, 128, 2} (B [N, K]); A as a 3-D view
+  // {64 (K), M, K/64} with box {64, m_pad, 2}.  Each lands exactly as two
+  // single-stage loads would.
+  CUtensorMap map_bt2;
+  CUtensorMap map_at2;
   CUtensorMap map_d;   // D [M, N], box {min(64, tile_n) (N), m_pad (rows)}, no swizzle
   CUtensorMap map_d2;  // D [M, N], box {tile_n - 64 (N), m_pad}, when tile_n > 64
   unsigned long long* err;
@@ -103,6 +116,9 @@ struct SmallMParams {
   int split;
   int b_kmajor;         // 1: B is stored [N, K]
   int staging_in_ring;  // 1: one tile per CTA, the output staging tile sits in the idle ring
+  int bt_boxes;         // loads per single stage of B^T (1 or 2), see map_bt
+  int pair_loads;       // 1: fill stages s, s+1 (s even) with map_bt2 / map_at2 where two
+                        // k-blocks of the segment remain
   void* d;            // D (split mode stores its rows directly)
   long long ldd;      // D's leading dimension, elements
   // Optional trace (nullptr: off): per CTA eight global-timer stamps (ns),

@@ -188,6 +188,25 @@ BWG_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int
       : "memory");
 }
 
+// 3-D and 4-D forms of the same load (coordinates innermost first).
+BWG_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                         int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+BWG_DEV void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                         int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 // Same, for a CTA pair: the completing barrier may live in the peer CTA
 // (`bar` is a shared::cluster address, e.g. from mapa_shared).
 BWG_DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,

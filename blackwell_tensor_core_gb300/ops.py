@@ -45,7 +45,8 @@ class PlanInfo(ctypes.Structure):
                 ("smem_total", ctypes.c_int), ("grid", ctypes.c_int), ("tx_bytes", ctypes.c_uint32),
                 ("idesc", ctypes.c_uint32), ("units", ctypes.c_int), ("streamk", ctypes.c_int),
                 ("workers", ctypes.c_int), ("dynamic", ctypes.c_int), ("sk_tiles", ctypes.c_int),
-                ("sk_segs", ctypes.c_int), ("split", ctypes.c_int), ("staging_in_ring", ctypes.c_int)]
+                ("sk_segs", ctypes.c_int), ("split", ctypes.c_int), ("staging_in_ring", ctypes.c_int),
+                ("bt_loads", ctypes.c_int), ("pair_loads", ctypes.c_int)]
 
 
 def lib() -> ctypes.CDLL:

@@ -336,6 +336,12 @@ typedef struct {
   int staging_in_ring;     /* SMALL_M: 1 if every CTA has one tile (or one slice of one
                               tile), so the output staging tile reuses the stage ring,
                               idle by then, and the ring is one stage deeper */
+  int bt_loads;            /* SMALL_M: TMA loads that fill one stage of B^T: 1 (B stored
+                              [N, K], or row-major B with N a multiple of 64, through a
+                              3-D view that takes both 64-channel halves at once) or 2 */
+  int pair_loads;          /* SMALL_M: 1 if pairs of ring stages are filled by one load of
+                              B^T and one of A (K a multiple of 64; for row-major B also
+                              N); each load carries a fixed cost, so this streams B faster */
 } bwg_plan_info;
 
 /*

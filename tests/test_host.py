@@ -200,6 +200,22 @@ def test_small_m_cluster_split_plan(ops, monkeypatch):
     assert ops.plan(72, 4096, 7168).split == 1 and ops.plan(72, 4096, 7168).streamk == 1
 
 
+def test_small_m_load_grouping_plan(ops, monkeypatch):
+    """How the small-M kernel fills its ring: one load of B^T a stage when the
+    3-D channel-group view tiles B (N a multiple of 64), else two; two stages
+    a load of B^T and of A when K (and N) are multiples of 64."""
+    cases = {(72, 16384, 7168): (1, 1), (72, 4096, 7168): (1, 1), (100, 1000, 640): (2, 0),
+             (33, 312, 1016): (2, 0), (72, 16384, 1000): (1, 0), (16, 2048, 4096): (1, 1),
+             (128, 4104, 640): (2, 0), (128, 4096, 640): (1, 1), (72, 1000, 448): (2, 0)}
+    for shape, (bt, pair) in cases.items():
+        p = ops.plan(*shape)
+        assert p.kernel == ops.KERNEL_SMALL_M and (p.bt_loads, p.pair_loads) == (bt, pair), shape
+    assert ops.plan(128, 4096, 640).stages == 7  # odd ring: the last stage is filled alone
+    assert ops.plan(256, 256, 256).pair_loads == 0  # not the small-M kernel
+    monkeypatch.setenv("BWG_SMALL_M_PAIRS", "0")
+    assert ops.plan(72, 16384, 7168).pair_loads == 0 and ops.plan(72, 16384, 7168).bt_loads == 1
+
+
 def test_instruction_descriptor_words(ops):
     # Fields (PTX ISA, tcgen05 instruction descriptor for kind::f16):
     # bit 4 = D is F32, bits 7-9 A format (1 = BF16), bits 10-12 B format,
