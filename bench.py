@@ -360,6 +360,15 @@ def cublas_context(ops, stream, dev, reps=40):
     D2 = torch.empty_like(D)
     ours = dense_launcher(ops, A, B, D, wl.OUT_BF16, stream)
     theirs = lambda: torch.matmul(A, B, out=D2)  # noqa: E731
+    mo, mc, n = alternate_with_cublas(ops, ours, theirs, stream, reps)
+    return {"ours_ms_median": mo, "cublas_ms_median": mc, "ours_tflops": c.flops / (mo * 1e-3) / 1e12,
+            "cublas_tflops": c.flops / (mc * 1e-3) / 1e12, "ours_over_cublas": mc / mo,
+            "launches_each": n}
+
+
+def alternate_with_cublas(ops, ours, theirs, stream, reps):
+    """Medians (ms) of CUDA-event times of `ours` and `theirs`, launched
+    alternately in blocks of 10 after three untimed launches of each."""
     for _ in range(3):
         ours()
         theirs()
@@ -368,10 +377,7 @@ def cublas_context(ops, stream, dev, reps=40):
         to += time_launches(ours, 10, stream, None, keep_ahead=True)[1]
         tc += time_launches(theirs, 10, stream, None, keep_ahead=True)[1]
     check_device_error(ops)
-    mo, mc = statistics.median(to), statistics.median(tc)
-    return {"ours_ms_median": mo, "cublas_ms_median": mc, "ours_tflops": c.flops / (mo * 1e-3) / 1e12,
-            "cublas_tflops": c.flops / (mc * 1e-3) / 1e12, "ours_over_cublas": mc / mo,
-            "launches_each": len(to)}
+    return statistics.median(to), statistics.median(tc), len(to)
 
 
 def _variant_small_m(ops, wl, stream, dist_mod, peaks, steps, warm, dev):
@@ -394,6 +400,11 @@ def _variant_small_m(ops, wl, stream, dist_mod, peaks, steps, warm, dev):
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": nbytes},
         "l2": "B (235 MB) larger than L2"}
+    # context: torch.matmul (cuBLAS) on the same inputs, alternated
+    D2 = torch.empty_like(D)
+    mo, mc, n = alternate_with_cublas(ops, launch, lambda: torch.matmul(A, B, out=D2), stream, 40)
+    out["small_m_72x16384x7168"]["context_cublas"] = {
+        "ours_ms_median": mo, "cublas_ms_median": mc, "ours_over_cublas": mc / mo, "launches_each": n}
     return out
 
 
