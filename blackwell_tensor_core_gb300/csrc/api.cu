@@ -202,14 +202,21 @@ int small_m_smem(int m_pad, int out_dtype, int stages, bool staging_in_ring = fa
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
-// Whether the small-M kernel fills its ring two stages per load: the views
-// that take two k-blocks (and, for row-major B, both channel halves) at once
-// tile the matrices exactly only when K (and N) are multiples of 64.
-// BWG_SMALL_M_PAIRS=0 turns it off.
-bool small_m_pairs_ok(int N, int K, int stages, bool b_kmajor) {
+// Whether the small-M kernel loads a stage of row-major B^T as one box of
+// the 3-D channel-group view: N must be a multiple of 64 (the groups tile B)
+// and so must the tile stride (every tile starts on a group).
+bool small_m_one_bt_box(int N, int tile_n, bool b_kmajor) {
+  return b_kmajor || (N % 64 == 0 && tile_n % 64 == 0);
+}
+
+// Whether it fills its ring two stages per load: the views that take two
+// k-blocks at once tile the matrices exactly only when K is a multiple of 64,
+// and for row-major B the stage must be one box.  BWG_SMALL_M_PAIRS=0 turns
+// it off.
+bool small_m_pairs_ok(int N, int K, int tile_n, int stages, bool b_kmajor) {
   const char* v = std::getenv("BWG_SMALL_M_PAIRS");
   if (v != nullptr && v[0] == '0') return false;
-  return K % 64 == 0 && stages >= 2 && (b_kmajor || N % 64 == 0);
+  return K % 64 == 0 && stages >= 2 && small_m_one_bt_box(N, tile_n, b_kmajor);
 }
 
 int group_m_from_env() {
@@ -345,8 +352,8 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     o->smem_input_per_cta = stages * small_m_stage_bytes(m_pad);
     o->smem_total = small_m_smem(m_pad, out_dtype, stages, in_ring);
     o->staging_in_ring = in_ring ? 1 : 0;
-    o->bt_loads = (b_kmajor || N % 64 == 0) ? 1 : 2;
-    o->pair_loads = small_m_pairs_ok(N, K, stages, b_kmajor) ? 1 : 0;
+    o->bt_loads = small_m_one_bt_box(N, o->tile_n, b_kmajor) ? 1 : 2;
+    o->pair_loads = small_m_pairs_ok(N, K, o->tile_n, stages, b_kmajor) ? 1 : 0;
     // each CTA's partial and the rows it receives fit in its idle stage ring
     if (split > 1 && (static_cast<long long>(m_pad) + static_cast<long long>(split) * ceil_div(M, split)) * 512 >
                          static_cast<long long>(stages) * small_m_stage_bytes(m_pad))
@@ -593,19 +600,19 @@ bool get_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dtype, uint64_
 
 // B^T maps of the small-M kernel (single stage and, where the layout
 // allows, two stages per load) and the two-stage map of A; sets bt_boxes and
-// pair_loads.  Row-major B with N not a multiple of 64 is loaded as two
-// 64-channel boxes a stage.
+// pair_loads.  Row-major B with N or the tile stride not a multiple of 64 is
+// loaded as two 64-channel boxes a stage.
 bool small_m_operand_maps(SmallMParams* p, const void* A, const void* B, CUtensorMapDataType in_t,
-                          int M, int N, int K, long long lda, long long ldb, int m_pad, int stages,
-                          bool b_kmajor) {
+                          int M, int N, int K, long long lda, long long ldb, int m_pad, int tile_n,
+                          int stages, bool b_kmajor) {
   const uint64_t bs = static_cast<uint64_t>(ldb) * 2;
   const uint64_t as = static_cast<uint64_t>(lda) * 2;
-  const bool pairs = small_m_pairs_ok(N, K, stages, b_kmajor);
+  const bool pairs = small_m_pairs_ok(N, K, tile_n, stages, b_kmajor);
   if (b_kmajor) {
     // B [N, K]: one box of 128 rows (channels) x 64 K a stage
     if (!get_map(&p->map_bt, B, in_t, K, N, bs, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
     p->bt_boxes = 1;
-  } else if (N % 64 == 0) {
+  } else if (small_m_one_bt_box(N, tile_n, false)) {
     const uint64_t dims[3] = {64, static_cast<uint64_t>(K), static_cast<uint64_t>(N / 64)};
     const uint64_t strides[2] = {bs, 128};
     const uint32_t box[3] = {64, 64, 2};
@@ -691,7 +698,8 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
     SmallMParams p;
     std::memset(&p, 0, sizeof(p));
     const int m_pad = pl.mma_n;
-    if (!small_m_operand_maps(&p, A, B, in_t, M, N, K, lda, ldb, m_pad, pl.stages, b_kmajor) ||
+    if (!small_m_operand_maps(&p, A, B, in_t, M, N, K, lda, ldb, m_pad, pl.tile_n, pl.stages,
+                              b_kmajor) ||
         !get_map(&p.map_at, A, in_t, K, M, static_cast<uint64_t>(lda) * 2, kBK, m_pad,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
         !get_map(&p.map_d, D, out_map_dtype(out_dtype), N, M, static_cast<uint64_t>(ldd) * oe,

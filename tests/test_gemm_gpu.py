@@ -371,20 +371,27 @@ def test_small_m_streamk_on_a_side_stream():
 
 @pytest.mark.parametrize("tile_n", [64, 80, 112, 128])
 @pytest.mark.parametrize("out", [wl.OUT_BF16, wl.OUT_FP32])
-def test_small_m_tile_stride(tile_n, out, monkeypatch):
+@pytest.mark.parametrize("N", [1000, 1024])
+def test_small_m_tile_stride(tile_n, out, N, monkeypatch):
     """Tiles that store fewer columns than the 128 the MMA spans: every
-    column written exactly once, ragged last tile clipped, padding untouched."""
+    column written exactly once, ragged last tile clipped, padding untouched.
+    With N = 1024 a stride of 64 or 128 loads B^T through the channel-group
+    view (one box a stage, two stages a load) and 80 or 112 as two boxes."""
+    from blackwell_tensor_core_gb300 import ops
     monkeypatch.setenv("BWG_SMALL_M_TILE_N", str(tile_n))
-    g = wl.generator(5800 + tile_n)
+    pl = ops.plan(72, N, 640, out)
+    grouped = N % 64 == 0 and tile_n % 64 == 0
+    assert (pl.bt_loads, pl.pair_loads) == ((1, 1) if grouped else (2, 0))
+    g = wl.generator(5800 + tile_n + N)
     A = wl.randint_matrix(72, 640, -2, 2, g)
-    B = wl.randint_matrix(640, 1000, -2, 2, g)
+    B = wl.randint_matrix(640, N, -2, 2, g)
     Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
-    D, full = gpu_gemm(A, B, out, None, ldd=1016, sentinel=5.0)
+    D, full = gpu_gemm(A, B, out, None, ldd=N + 16, sentinel=5.0)
     if out == wl.OUT_FP32:
         assert np.array_equal(D.double().numpy(), Dref)
     else:
         assert_bits_equal(D, oracle.round_to(Dref, "bf16"), "tile_n %d" % tile_n)
-    assert torch.all(full[:, 1000:] == 5.0)
+    assert torch.all(full[:, N:] == 5.0)
 
 
 @pytest.mark.parametrize("shape", [(512, 256, 512), (520, 600, 456), (1000, 136, 1000), (1536, 2304, 640),

@@ -212,6 +212,12 @@ def test_small_m_load_grouping_plan(ops, monkeypatch):
         assert p.kernel == ops.KERNEL_SMALL_M and (p.bt_loads, p.pair_loads) == (bt, pair), shape
     assert ops.plan(128, 4096, 640).stages == 7  # odd ring: the last stage is filled alone
     assert ops.plan(256, 256, 256).pair_loads == 0  # not the small-M kernel
+    # the channel-group view needs every tile to start on a group of 64
+    for tile_n, want in ((64, (1, 1)), (80, (2, 0)), (112, (2, 0)), (128, (1, 1))):
+        monkeypatch.setenv("BWG_SMALL_M_TILE_N", str(tile_n))
+        p = ops.plan(72, 1024, 640)
+        assert p.tile_n == tile_n and (p.bt_loads, p.pair_loads) == want, tile_n
+    monkeypatch.delenv("BWG_SMALL_M_TILE_N")
     monkeypatch.setenv("BWG_SMALL_M_PAIRS", "0")
     assert ops.plan(72, 16384, 7168).pair_loads == 0 and ops.plan(72, 16384, 7168).bt_loads == 1
 
