@@ -12,11 +12,11 @@
 // k are contiguous: the MMA's A operand is MN-major, two 64-channel x 64-K
 // blocks with 128-byte swizzle, taken by one load through a 3-D view of B
 // (64 channels, k, channel group).  A is row-major [M,K]: the MMA's B operand
-// is K-major, one box of m_pad rows x 64 K.  Each TMA load has a fixed cost
-// on the SM besides its bytes, and measured on GB300 this kernel streams B at
-// a rate set by the loads per byte: two 64x64 boxes a stage ran 8% slower
-// than one 3-D load, and filling two stages per load (4-D view of B, 3-D of
-// A) gained 8% more.  The accumulator has TMEM lane = output column and
+// is K-major, one box of m_pad rows x 64 K.  Measured on GB300, this kernel
+// streams B faster the fewer TMA loads it issues per byte: two 64x64 boxes a
+// stage ran 8% slower than one 3-D load, and filling two stages per load
+// (4-D view of B, 3-D of A) gained up to 8% more, depending on the shape and
+// the GPU.  The accumulator has TMEM lane = output column and
 // TMEM column = row of D, so each epilogue thread owns one output column and
 // writes it down the rows of a [m_pad x 64] staging tile, which a TMA store
 // then writes to D (rows >= M are clipped by the tensor bounds).  No transpose
@@ -174,11 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
   // the first ring stages before the block-wide barrier below: the first
   // loads are in flight while TMEM is being allocated.
   //
-  // Each TMA load costs the SM a fixed amount of time besides its bytes:
-  // this kernel streams B at a rate set by how many loads it issues per
-  // byte, not by the bytes alone.  So a stage of B^T is one load where the
-  // layout allows it, and with pair_loads two stages are filled by one load
-  // of B^T and one of A.  The pair completes on the first stage's barrier;
+  // Fewer, larger loads stream B faster, so a stage of B^T is one load
+  // where the layout allows it, and with pair_loads two stages are filled by
+  // one load of B^T and one of A.  The pair completes on the first stage's barrier;
   // the second stage's barrier gets a plain arrival.  The MMA issuer takes
   // the stages in order, so it has waited for the pair's bytes before it
   // reads the second stage.
