@@ -283,6 +283,7 @@ void bwg_debug_set_trace(void* buffer);
  *   BWG_SMALL_M_TILE_N output columns per small-M tile (16..128, default 128)
  *   BWG_SMALL_M_SPLIT  0: no cluster split; F (2..8): that cluster size
  *   BWG_STREAMK        1 / 0: force stream-K on / off in the small-M kernel
+ *   BWG_SMALL_M_PAIRS  0: fill the small-M stage ring one stage per load
  *   BWG_GROUPED_1C     1: grouped kernels with one MMA consumer (256-row units)
  *   BWG_GROUPED_SWAP   1: swapped-operand group ends (one-consumer grouped kernel)
  * ------------------------------------------------------------------- */
