@@ -168,6 +168,10 @@ def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None,
         out = torch.empty((M, N), dtype=out_dtype, device=A.device)
     if out.dtype not in _OUT_CODES:
         raise TypeError("output dtype must be bfloat16, float16 or float32")
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must be [%d, %d], got %s" % (M, N, tuple(out.shape)))
+    if not (A.device == B.device == out.device):
+        raise ValueError("A, B and out must be on the same device")
     lda, ldb, ldd = _matrix(A, "A"), _matrix(B, "B"), _matrix(out, "out")
     if b_transposed:
         fn = gemm_bf16_nt if A.dtype == torch.bfloat16 else gemm_fp16_nt
@@ -271,6 +275,18 @@ def gemm_bf16_host(A_host: torch.Tensor, B_host: torch.Tensor, D_host: torch.Ten
     N = B_host.shape[1]
     if D_host.dtype not in _OUT_CODES:
         raise TypeError("output dtype must be bfloat16, float16 or float32")
+    if A_host.dtype != torch.bfloat16 or B_host.dtype != torch.bfloat16:
+        raise TypeError("A_host and B_host must be bfloat16")
+    if B_host.shape[0] != K or tuple(D_host.shape) != (M, N):
+        raise ValueError("shapes must be A [M, K], B [K, N], D [M, N]; got %s, %s, %s"
+                         % (tuple(A_host.shape), tuple(B_host.shape), tuple(D_host.shape)))
+    for name, t in (("A_host", A_host), ("B_host", B_host), ("D_host", D_host)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a dense host tensor" % name)
+    need = {"dA": M * K * 2, "dB": K * N * 2, "dD": M * N * D_host.element_size()}
+    for name, t in (("dA", dA), ("dB", dB), ("dD", dD)):
+        if not t.is_cuda or not t.is_contiguous() or t.numel() * t.element_size() < need[name]:
+            raise ValueError("%s must be a dense CUDA buffer of at least %d bytes" % (name, need[name]))
     _check(lib().gemm_bf16_host(A_host.data_ptr(), B_host.data_ptr(), D_host.data_ptr(), M, N, K,
                                 _OUT_CODES[D_host.dtype], dA.data_ptr(), dB.data_ptr(), dD.data_ptr(),
                                 _stream_handle(stream, dA.device)), "gemm_bf16_host")

@@ -417,3 +417,45 @@ def test_quarter_split_for_two_consumer_tiles(ops, T, C):
         got = sorted(seen[t])
         n = got[0][1]
         assert got == [(k, n) for k in range(n)]
+
+
+def test_gemm_binding_rejects_bad_tensors_before_any_call(ops):
+    """The torch-level wrapper checks shapes and dtypes on the host, so a
+    wrong output buffer never reaches the kernels (an `out` with fewer rows
+    than M would otherwise be written past its end)."""
+    import torch
+    A = torch.zeros((72, 64), dtype=torch.bfloat16)
+    B = torch.zeros((64, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match=r"out must be \[72, 128\]"):
+        ops.gemm(A, B, out=torch.zeros((71, 128), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match=r"out must be \[72, 128\]"):
+        ops.gemm(A, B, out=torch.zeros((72, 120), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="inner dimensions"):
+        ops.gemm(A, torch.zeros((65, 128), dtype=torch.bfloat16))
+    with pytest.raises(TypeError):
+        ops.gemm(A, B.to(torch.float16))
+    with pytest.raises(TypeError):
+        ops.gemm(A, B, out=torch.zeros((72, 128), dtype=torch.float64))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        ops.gemm(A, B)  # host tensors: the library works on device memory only
+
+
+def test_host_buffer_binding_checks_shapes_and_buffers(ops):
+    """gemm_bf16_host takes raw pointers; its wrapper checks the host
+    tensors' shapes and dtypes and that the device buffers are CUDA buffers
+    large enough for A, B and D before calling it."""
+    import torch
+    hA = torch.zeros((64, 32), dtype=torch.bfloat16)
+    hB = torch.zeros((32, 48), dtype=torch.bfloat16)
+    hD = torch.zeros((64, 48), dtype=torch.bfloat16)
+    dev = [torch.zeros(1, dtype=torch.uint8)] * 3
+    with pytest.raises(ValueError, match="shapes must be"):
+        ops.gemm_bf16_host(hA, hB, torch.zeros((64, 40), dtype=torch.bfloat16), *dev)
+    with pytest.raises(ValueError, match="shapes must be"):
+        ops.gemm_bf16_host(hA, torch.zeros((33, 48), dtype=torch.bfloat16), hD, *dev)
+    with pytest.raises(TypeError):
+        ops.gemm_bf16_host(hA.half(), hB, hD, *dev)
+    with pytest.raises(ValueError, match="dense host tensor"):
+        ops.gemm_bf16_host(hA.t().contiguous().t(), hB, hD, *dev)
+    with pytest.raises(ValueError, match="dA must be a dense CUDA buffer of at least 4096 bytes"):
+        ops.gemm_bf16_host(hA, hB, hD, *dev)
