@@ -21,6 +21,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -217,9 +218,15 @@ def time_launches(launch, steps, stream, dist_mod, between=None, keep_ahead=Fals
     return t0.elapsed_time(t1), [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def launch_stats(per):
-    """Median, min and max of per-launch times (ms)."""
-    return {"median": statistics.median(per), "min": min(per), "max": max(per), "launches": len(per)}
+def launch_stats(per, window=20):
+    """Median, min and max of per-launch times (ms), and the lowest and
+    highest mean over `window` consecutive launches (the MegaMoE page's
+    windowed average of back-to-back launches)."""
+    out = {"median": statistics.median(per), "min": min(per), "max": max(per), "launches": len(per)}
+    if len(per) >= window:
+        sums = [math.fsum(per[i:i + window]) for i in range(len(per) - window + 1)]
+        out["window_mean_%d" % window] = {"min": min(sums) / window, "max": max(sums) / window}
+    return out
 
 
 def toolchain():
@@ -603,9 +610,9 @@ def run_ours(args, rank, world, local):
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
-        "launch_ms": {"mean": mean_launch, "median": statistics.median(per), "min": min(per), "max": max(per),
-                      "first_tenth_mean": statistics.mean(per[:max(1, len(per) // 10)]),
-                      "last_tenth_mean": statistics.mean(per[-max(1, len(per) // 10):])},
+        "launch_ms": dict(launch_stats(per), mean=mean_launch,
+                          first_tenth_mean=statistics.mean(per[:max(1, len(per) // 10)]),
+                          last_tenth_mean=statistics.mean(per[-max(1, len(per) // 10):])),
         "variants": variants,
         "variants_clocks": variant_clocks,
         "context_cublas": context,

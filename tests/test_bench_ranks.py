@@ -68,3 +68,17 @@ def test_warmup_below_three_is_rejected():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"],
                        capture_output=True, text=True, timeout=120)
     assert r.returncode != 0
+
+
+def test_launch_stats_window_means():
+    """Windowed means of consecutive launches: exact on a known sequence,
+    absent when there are fewer launches than one window."""
+    sys.path.insert(0, ROOT)
+    import bench
+    per = [1.0] * 20 + [3.0] * 20
+    st = bench.launch_stats(per)
+    assert st["median"] == 2.0 and st["min"] == 1.0 and st["max"] == 3.0 and st["launches"] == 40
+    assert st["window_mean_20"] == {"min": 1.0, "max": 3.0}
+    st = bench.launch_stats([2.0, 4.0, 6.0, 8.0], window=2)
+    assert st["window_mean_2"] == {"min": 3.0, "max": 7.0}
+    assert "window_mean_20" not in bench.launch_stats([1.0] * 19)
