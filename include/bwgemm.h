@@ -338,11 +338,12 @@ typedef struct {
                               tile), so the output staging tile reuses the stage ring,
                               idle by then, and the ring is one stage deeper */
   int bt_loads;            /* SMALL_M: TMA loads that fill one stage of B^T: 1 (B stored
-                              [N, K], or row-major B with N a multiple of 64, through a
-                              3-D view that takes both 64-channel halves at once) or 2 */
+                              [N, K], or row-major B with N and tile_n multiples of 64,
+                              through a 3-D view that takes both 64-channel halves at
+                              once) or 2 */
   int pair_loads;          /* SMALL_M: 1 if pairs of ring stages are filled by one load of
-                              B^T and one of A (K a multiple of 64; for row-major B also
-                              N); each load carries a fixed cost, so this streams B faster */
+                              B^T and one of A (K a multiple of 64, and bt_loads = 1);
+                              fewer, larger loads measured faster on GB300 */
 } bwg_plan_info;
 
 /*
