@@ -1,29 +1,36 @@
 #!/usr/bin/env python3
-"""Benchmark of the GEMM hot path on GB300.
+"""Benchmark of the GEMM hot path on one GB300.
 
 Metric: GEMM TFLOP/s at M = N = K = 8192, BF16 inputs U[-1,1], FP32
 accumulation, BF16 output, device-timed with CUDA events, and its fraction of
 the dense BF16 tensor peak.  One step = one gemm_bf16 call through the C ABI
 on that workload (host validation, planning, descriptors, the persistent
-2-CTA kernel).  The inputs (256 MiB of A and B) are larger than the 129 MB L2,
-so no flush is needed between timed iterations.
+CTA-pair kernel).  The inputs (256 MiB of A and B) are larger than the 129 MB
+L2, so no flush is needed between timed iterations.
 
-Prints ONE JSON line (rank 0).  Flags: --gpus N --steps K --warmup W
-[--impl reference] [--no-variants].  Under torchrun every rank runs its own
-replica of the workload (the product has no exchange step at one GPU per
-problem) and the slowest rank's time sets the aggregate.
+Prints ONE JSON line.  Flags: --gpus N --steps K --warmup W
+[--impl reference] [--no-variants] [--no-cpu-baseline].
+
+The library runs on one GPU only: its multicast kernel may read only the
+memory of the GPU it runs on, and no part of it exchanges data between GPUs.
+So this benchmark refuses --gpus above 1 and any launch with WORLD_SIZE above
+1 (status 2, before any GPU work).
+
+After the K timed steps the same launch runs back to back for at least two
+seconds (the "sustained" object: the GPU settles at its power cap there, so
+that figure is compared with the sustained peak).  The other method workloads
+follow as "variants", each with its own oracle timing on the host cores.
 
 --impl reference times the CPU oracle (FP64 triple loop, test infrastructure)
-on a bounded sample of rows of the same product, on this machine's host cores.
+on a bounded sample of rows of the same product, on this machine's host cores
+(rank 0 only under a multi-rank launcher; the other ranks exit without work).
 """
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import math
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -37,10 +44,22 @@ if ROOT not in sys.path:
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "GEMM TFLOPS at 8192^3 BF16 (device-timed) and % of dense BF16 tensor peak"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_gemm_8192.txt")
+# Sources of the benchmark's kernel (the dense two-consumer pair kernel and
+# the host code that launches it): the committed DRAM traffic figure is
+# reported only while their code-only hash matches the one it was taken on.
 KERNEL_SOURCES = ["gemm_tc.cu", "ptx.cuh", "layout.h", "params.h", "api.cu"]
 KERNEL_NAMES = {2: "persistent 1-CTA", 3: "persistent CTA pair (cta_group::2)",
                 4: "swapped small-M", 5: "two pairs sharing B by TMA multicast",
                 6: "persistent CTA pair, two MMA consumers (cta_group::2)"}
+ONE_GPU = ("one GPU only: the library's kernels run on a single GPU (its multicast loads may read "
+           "only that GPU's memory) and it has no multi-GPU path")
+SUSTAINED_S = 2.2
+# The workload, identical in both arms' lines.
+CONFIG = {"workload": "gemm_8192x8192x8192_bf16in_fp32acc_bf16out", "M": 8192, "N": 8192, "K": 8192,
+          "inputs": "U[-1,1], seed 1003, row-major A and B",
+          "layout": "A [M,K] and B [K,N] row-major, D [M,N] row-major",
+          "l2": "inputs larger than L2 (A+B = 256 MiB > 129 MB); no flush",
+          "parallelism": "single GPU"}
 
 
 # ----------------------------------------------------------------- infra ----
@@ -48,30 +67,7 @@ KERNEL_NAMES = {2: "persistent 1-CTA", 3: "persistent CTA pair (cta_group::2)",
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return rank, world, local
-
-
-def init_dist(world: int, backend: str):
-    import torch.distributed as dist
-    if world > 1 and not dist.is_initialized():
-        dist.init_process_group(backend=backend)
-    return dist if world > 1 else None
-
-
-def barrier(dist_mod):
-    if dist_mod is not None:
-        dist_mod.barrier()
-
-
-def max_over_ranks(value: float, dist_mod, device) -> float:
-    """The largest value any rank holds (slowest rank's time)."""
-    if dist_mod is None:
-        return value
-    import torch
-    t = torch.tensor([value], dtype=torch.float64, device=device)
-    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
-    return float(t.item())
+    return rank, world
 
 
 def load_peaks():
@@ -152,23 +148,18 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
-def _code_only(text: str) -> str:
-    """C/C++/CUDA source with comments and blank space removed, so that the
-    hash below changes with the code, not with its comments."""
-    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-    text = re.sub(r"//[^\n]*", " ", text)
-    return " ".join(text.split())
-
-
 def kernel_source_hash(read=None) -> str:
+    """Code-only hash of the benchmark kernel's sources (KERNEL_SOURCES)."""
+    import hashlib
+    from blackwell_tensor_core_gb300 import build
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
         if read is None:
-            with open(os.path.join(ROOT, "blackwell_tensor_core_gb300", "csrc", name), encoding="utf-8") as f:
+            with open(os.path.join(build.CSRC, name), encoding="utf-8") as f:
                 text = f.read()
         else:
             text = read(name)
-        h.update(_code_only(text).encode())
+        h.update(build.code_only(text).encode())
     return h.hexdigest()[:16]
 
 
@@ -191,7 +182,7 @@ def recorded_traffic():
 
 # ------------------------------------------------------------- timing -------
 
-def time_launches(launch, steps, stream, dist_mod, between=None, keep_ahead=False):
+def time_launches(launch, steps, stream, between=None, keep_ahead=False):
     """Times `steps` launches on `stream`.  Returns (total_ms, per-launch ms list).
     keep_ahead: a GPU sleep before the first timed launch lets the host queue
     the launches ahead of the GPU, so that short kernels are timed without
@@ -201,20 +192,18 @@ def time_launches(launch, steps, stream, dist_mod, between=None, keep_ahead=Fals
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    barrier(dist_mod)
     torch.cuda.synchronize()
     if keep_ahead:
         torch.cuda._sleep(min(2_000_000 + 20_000 * steps, 40_000_000))
     t0.record(stream)
     for i in range(steps):
         if between is not None:
-            between()
+            between(i)
         starts[i].record(stream)
-        launch()
+        launch(i)
         ends[i].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
-    barrier(dist_mod)
     return t0.elapsed_time(t1), [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
@@ -242,10 +231,19 @@ def toolchain():
 
 
 def dense_launcher(ops, A, B, D, out_code, stream):
-    M, K = A.shape
-    N = B.shape[1]
-    a, b, d, h = A.data_ptr(), B.data_ptr(), D.data_ptr(), stream.cuda_stream
-    return lambda: ops.gemm_bf16(a, b, d, M, N, K, K, N, N, out_code, h)
+    """launch(i) -> one gemm_bf16 call.  A and B may be lists of equally
+    shaped input sets, taken in turn (rotating buffers)."""
+    As = A if isinstance(A, (list, tuple)) else [A]
+    Bs = B if isinstance(B, (list, tuple)) else [B]
+    M, K = As[0].shape
+    N = Bs[0].shape[1]
+    ptrs = [(a.data_ptr(), b.data_ptr()) for a, b in zip(As, Bs)]
+    d, h = D.data_ptr(), stream.cuda_stream
+
+    def launch(i=0):
+        a, b = ptrs[i % len(ptrs)]
+        ops.gemm_bf16(a, b, d, M, N, K, K, N, N, out_code, h)
+    return launch
 
 
 def check_device_error(ops):
@@ -254,92 +252,99 @@ def check_device_error(ops):
         raise RuntimeError("device error word %#x (status %d)" % (word, st))
 
 
-# ---------------------------------------------------------------- arms ------
+# ------------------------------------------------------------ oracle --------
 
-def oracle_rows_tflops(A_bits, B_bits, rows, start_row=0):
+def oracle_rate(A_bits, B_bits, budget_s, max_rows=None, threads=None, what=""):
+    """The oracle as it stands, on blocks of rows of A x B in order, until
+    about `budget_s` seconds of work (or `max_rows` rows).  Returns the
+    cpu_baseline object (TFLOP/s over the rows done, 2 * rows * N * K)."""
     import oracle
-    t0 = time.perf_counter()
-    oracle.gemm(A_bits, B_bits, rows=(start_row, start_row + rows))
-    dt = time.perf_counter() - t0
-    K = A_bits.shape[1]
-    N = B_bits.shape[1]
-    return 2.0 * rows * N * K / dt / 1e12, dt
+    oracle.build()
+    all_threads = oracle.num_threads()
+    if threads is not None:
+        oracle.set_num_threads(threads)
+    try:
+        cores = oracle.num_threads()
+        M, K = A_bits.shape
+        N = B_bits.shape[1]
+        limit = M if max_rows is None else min(M, max_rows)
+        oracle.gemm(A_bits, B_bits, rows=(0, min(2, limit)))  # load the library, touch the inputs
+        block = max(1, min(limit, 2 * cores))
+        rows, dt = 0, 0.0
+        while dt < budget_s and rows < limit:
+            n = min(block, limit - rows)
+            t0 = time.perf_counter()
+            oracle.gemm(A_bits, B_bits, rows=(rows, rows + n))
+            dt += time.perf_counter() - t0
+            rows += n
+    finally:
+        oracle.set_num_threads(all_threads)
+    return {"value": 2.0 * rows * N * K / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": "%s%d of %d rows of the %dx%dx%d product (%d outputs), FP64, %.1f s"
+                      % (what, rows, M, M, N, K, rows * N, dt)}
 
 
 def cpu_baseline(case, budget_s=12.0):
-    """The oracle as it stands on a bounded row sample of the same product:
-    blocks of rows, in order, until about `budget_s` seconds of work."""
-    import oracle
+    """The oracle on a bounded row sample of the benchmark product."""
     from blackwell_tensor_core_gb300 import workloads as wl
-    oracle.build()
-    Ab, Bb = wl.bits(case.A), wl.bits(case.B)
-    oracle_rows_tflops(Ab, Bb, 4)  # load the library, touch the inputs
-    rows, dt, start = 0, 0.0, 0
-    block = 2 * oracle.num_threads()
-    while dt < budget_s and start + block <= case.M:
-        _, t = oracle_rows_tflops(Ab, Bb, block, start)
-        rows += block
-        dt += t
-        start += block
-    val = 2.0 * rows * case.N * case.K / dt / 1e12
-    return {"value": val, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "%d rows of the %dx%dx%d product (%d outputs, K=%d), FP64, %.1f s"
-                      % (rows, case.M, case.N, case.K, rows * case.N, case.K, dt)}
+    return oracle_rate(wl.bits(case.A), wl.bits(case.B), budget_s)
 
 
-def run_reference(args, rank):
-    """Reference arm: the CPU oracle on a bounded sample per step (rank 0 only)."""
-    if rank != 0:
-        return
+def run_reference(args):
+    """Reference arm: the CPU oracle on a bounded sample per step."""
     import oracle
     from blackwell_tensor_core_gb300 import workloads as wl
     oracle.build()
     case = wl.large_case()
     Ab, Bb = wl.bits(case.A), wl.bits(case.B)
-    _, dt = oracle_rows_tflops(Ab, Bb, 2)
-    per_row = dt / 2
+
+    def rows_once(rows, start):
+        t0 = time.perf_counter()
+        oracle.gemm(Ab, Bb, rows=(start, start + rows))
+        return time.perf_counter() - t0
+
+    per_row = rows_once(2, 0) / 2
     rows = max(1, int(120.0 / max((args.steps + args.warmup) * per_row, 1e-9)))
     rows = min(rows, case.M)
     for i in range(args.warmup):
-        oracle_rows_tflops(Ab, Bb, rows, (i * rows) % (case.M - rows + 1))
-    vals, times = [], []
-    for i in range(args.steps):
-        v, dt = oracle_rows_tflops(Ab, Bb, rows, ((args.warmup + i) * rows) % (case.M - rows + 1))
-        vals.append(v)
-        times.append(dt)
+        rows_once(rows, (i * rows) % (case.M - rows + 1))
+    times = [rows_once(rows, ((args.warmup + i) * rows) % (case.M - rows + 1)) for i in range(args.steps)]
     value = 2.0 * rows * case.N * case.K * len(times) / sum(times) / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "gemm_8192x8192x8192 (oracle, %d-row sample per step)" % rows,
-                   "M": case.M, "N": case.N, "K": case.K},
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": dict(CONFIG),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
                          "kind": "oracle",
-                         "sample": "%d rows of the 8192^3 product per step, FP64 triple loop" % rows},
+                         "sample": "%d rows of the 8192^3 product per step (%d outputs, K=8192), "
+                                   "FP64 triple loop" % (rows, rows * case.N)},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def measure_variants(ops, wl, stream, dist_mod, peaks, steps, only=None, warm=5):
+# ----------------------------------------------------------- variants -------
+
+def measure_variants(ops, wl, stream, peaks, steps, only=None, warm=5):
     """Shorter measurements of the other method workloads (same JSON line)."""
     import torch
     out = {}
     dev = torch.device("cuda")
     if only in (None, "tile"):
-        out.update(_variant_tile(ops, wl, stream, dist_mod, steps, warm, dev))
+        out.update(_variant_tile(ops, wl, stream, steps, warm, dev))
     if only in (None, "small_m"):
-        out.update(_variant_small_m(ops, wl, stream, dist_mod, peaks, steps, warm, dev))
+        out.update(_variant_small_m(ops, wl, stream, peaks, steps, warm, dev))
     if only in (None, "square"):
-        out.update(_variant_square(ops, wl, stream, dist_mod, peaks, steps, warm, dev))
+        out.update(_variant_square(ops, wl, stream, peaks, steps, warm, dev))
+    if only in (None, "large_cold"):
+        out.update(_variant_large_cold(ops, wl, stream, peaks, steps, warm, dev))
     if only in (None, "grouped"):
-        out.update(_variant_grouped(ops, wl, stream, dist_mod, peaks, steps, warm, dev))
+        out.update(_variant_grouped(ops, wl, stream, peaks, steps, warm, dev))
     return out
 
 
-def _variant_tile(ops, wl, stream, dist_mod, steps, warm, dev):
+def _variant_tile(ops, wl, stream, steps, warm, dev):
     """The one-tile integer case (256x256x512, FP32 out): a latency figure."""
     import torch
     c = wl.tile_case()
@@ -348,7 +353,7 @@ def _variant_tile(ops, wl, stream, dist_mod, steps, warm, dev):
     launch = dense_launcher(ops, A, B, D, wl.OUT_FP32, stream)
     for _ in range(warm):
         launch()
-    _, per = time_launches(launch, steps, stream, dist_mod, keep_ahead=True)
+    _, per = time_launches(launch, steps, stream, keep_ahead=True)
     check_device_error(ops)
     return {"tile_256x256x512_fp32out": {"ms_per_launch_median": statistics.median(per),
                                          "ms_per_launch_min": min(per),
@@ -366,7 +371,7 @@ def cublas_context(ops, stream, dev, reps=40):
     D = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=dev)
     D2 = torch.empty_like(D)
     ours = dense_launcher(ops, A, B, D, wl.OUT_BF16, stream)
-    theirs = lambda: torch.matmul(A, B, out=D2)  # noqa: E731
+    theirs = lambda i=0: torch.matmul(A, B, out=D2)  # noqa: E731
     mo, mc, n = alternate_with_cublas(ops, ours, theirs, stream, reps)
     return {"ours_ms_median": mo, "cublas_ms_median": mc, "ours_tflops": c.flops / (mo * 1e-3) / 1e12,
             "cublas_tflops": c.flops / (mc * 1e-3) / 1e12, "ours_over_cublas": mc / mo,
@@ -381,13 +386,13 @@ def alternate_with_cublas(ops, ours, theirs, stream, reps):
         theirs()
     to, tc = [], []
     for _ in range(reps // 10):
-        to += time_launches(ours, 10, stream, None, keep_ahead=True)[1]
-        tc += time_launches(theirs, 10, stream, None, keep_ahead=True)[1]
+        to += time_launches(ours, 10, stream, keep_ahead=True)[1]
+        tc += time_launches(theirs, 10, stream, keep_ahead=True)[1]
     check_device_error(ops)
     return statistics.median(to), statistics.median(tc), len(to)
 
 
-def _variant_small_m(ops, wl, stream, dist_mod, peaks, steps, warm, dev):
+def _variant_small_m(ops, wl, stream, peaks, steps, warm, dev):
     import torch
     out = {}
     # small-M swapped kernel: HBM-bound, report algorithmic GB/s
@@ -397,25 +402,25 @@ def _variant_small_m(ops, wl, stream, dist_mod, peaks, steps, warm, dev):
     launch = dense_launcher(ops, A, B, D, wl.OUT_BF16, stream)
     for _ in range(warm):
         launch()
-    _, per = time_launches(launch, steps, stream, dist_mod, keep_ahead=True)
+    _, per = time_launches(launch, steps, stream, keep_ahead=True)
     check_device_error(ops)
     ms = statistics.mean(per)
     nbytes = 2 * (c.M * c.K + c.K * c.N + c.M * c.N)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    out["small_m_72x16384x7168"] = {
-        "ms_per_launch": ms, "tflops": c.flops / (ms * 1e-3) / 1e12, "launch_ms": launch_stats(per),
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": nbytes},
-        "l2": "B (235 MB) larger than L2"}
+    v = {"ms_per_launch": ms, "tflops": c.flops / (ms * 1e-3) / 1e12, "launch_ms": launch_stats(per),
+         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                      "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": nbytes},
+         "l2": "B (235 MB) larger than L2"}
     # context: torch.matmul (cuBLAS) on the same inputs, alternated
     D2 = torch.empty_like(D)
-    mo, mc, n = alternate_with_cublas(ops, launch, lambda: torch.matmul(A, B, out=D2), stream, 40)
-    out["small_m_72x16384x7168"]["context_cublas"] = {
-        "ours_ms_median": mo, "cublas_ms_median": mc, "ours_over_cublas": mc / mo, "launches_each": n}
+    mo, mc, n = alternate_with_cublas(ops, launch, lambda i=0: torch.matmul(A, B, out=D2), stream, 40)
+    v["context_cublas"] = {"ours_ms_median": mo, "cublas_ms_median": mc, "ours_over_cublas": mc / mo,
+                           "launches_each": n}
+    out["small_m_72x16384x7168"] = v
     return out
 
 
-def _variant_square(ops, wl, stream, dist_mod, peaks, steps, warm, dev):
+def _variant_square(ops, wl, stream, peaks, steps, warm, dev):
     import torch
     out = {}
     # square 4096: inputs fit in L2, so flush L2 between timed launches
@@ -426,7 +431,7 @@ def _variant_square(ops, wl, stream, dist_mod, peaks, steps, warm, dev):
     launch = dense_launcher(ops, A, B, D, wl.OUT_BF16, stream)
     for _ in range(warm):
         launch()
-    _, per = time_launches(launch, steps, stream, dist_mod, between=lambda: flush.zero_())
+    _, per = time_launches(launch, steps, stream, between=lambda i: flush.zero_())
     check_device_error(ops)
     ms = statistics.mean(per)
     tf = c.flops / (ms * 1e-3) / 1e12
@@ -437,10 +442,34 @@ def _variant_square(ops, wl, stream, dist_mod, peaks, steps, warm, dev):
     return out
 
 
-def _variant_grouped(ops, wl, stream, dist_mod, peaks, steps, warm, dev):
+def _variant_large_cold(ops, wl, stream, peaks, steps, warm, dev):
+    """The benchmark product on two rotating input sets (512 MiB of A and B),
+    so that no launch finds its inputs in L2 from the launch before."""
+    import torch
+    c = wl.large_case()
+    c2 = wl.large_case(seed=2003)
+    As = [c.A.to(dev), c2.A.to(dev)]
+    Bs = [c.B.to(dev), c2.B.to(dev)]
+    D = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=dev)
+    launch = dense_launcher(ops, As, Bs, D, wl.OUT_BF16, stream)
+    for i in range(warm):
+        launch(i)
+    _, per = time_launches(launch, steps, stream)
+    check_device_error(ops)
+    ms = statistics.mean(per)
+    tf = c.flops / (ms * 1e-3) / 1e12
+    return {"large_8192_rotating": {
+        "ms_per_launch": ms, "tflops": tf, "launch_ms": launch_stats(per),
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tf / peaks["bf16_tflops"]},
+        "l2": "two input sets (2 x 256 MiB) taken in turn: cold L2 for every launch"}}
+
+
+def _variant_grouped(ops, wl, stream, peaks, steps, warm, dev):
     """Grouped expert FC1, FC1 + SwiGLU and FC2, launched in alternating blocks
     of ten so that the three see the same clocks (after the long 8192^3 loop
-    the GPU runs at its power cap, and the clock drifts as it warms)."""
+    the GPU runs at its power cap, and the clock drifts as it warms); then
+    FC1 on two rotating input sets."""
     import torch
     out = {}
     c = wl.grouped_case()
@@ -459,13 +488,15 @@ def _variant_grouped(ops, wl, stream, dist_mod, peaks, steps, warm, dev):
     b2ptrs = [b.data_ptr() for b in B2]
     a2, d2 = A2.data_ptr(), D2.data_ptr()
     launches = {
-        "grouped_fc1_32x4096x4096": (lambda: ops.grouped_gemm_bf16(a, bptrs, d, o, c.G, c.total, c.N, c.K, h),
-                                     c.flops, {"rows": c.total, "l2": "A + B (1.34 GB) larger than L2"}),
+        "grouped_fc1_32x4096x4096": (
+            lambda i=0: ops.grouped_gemm_bf16(a, bptrs, d, o, c.G, c.total, c.N, c.K, h),
+            c.flops, {"rows": c.total, "l2": "A + B (1.34 GB) larger than L2"}),
         "grouped_fc1_swiglu_32x4096x4096": (
-            lambda: ops.grouped_gemm_swiglu_bf16(a, bptrs, hp, o, c.G, c.total, c.N, c.K, h), c.flops,
+            lambda i=0: ops.grouped_gemm_swiglu_bf16(a, bptrs, hp, o, c.G, c.total, c.N, c.K, h), c.flops,
             {"rows": c.total, "out_cols": c.N // 2, "l2": "A + B (1.34 GB) larger than L2"}),
-        "grouped_fc2_32x4096x2048": (lambda: ops.grouped_gemm_bf16(a2, b2ptrs, d2, o, c2.G, c2.total, c2.N, c2.K, h),
-                                     c2.flops, {"rows": c2.total, "l2": "A + B (0.67 GB) larger than L2"}),
+        "grouped_fc2_32x4096x2048": (
+            lambda i=0: ops.grouped_gemm_bf16(a2, b2ptrs, d2, o, c2.G, c2.total, c2.N, c2.K, h),
+            c2.flops, {"rows": c2.total, "l2": "A + B (0.67 GB) larger than L2"}),
     }
     for fn, _, _ in launches.values():
         for _ in range(warm):
@@ -475,7 +506,7 @@ def _variant_grouped(ops, wl, stream, dist_mod, peaks, steps, warm, dev):
     for _ in range(blocks):
         for k, (fn, _, _) in launches.items():
             fn()  # one untimed launch after each switch of workload
-            per[k] += time_launches(fn, 10, stream, dist_mod)[1]
+            per[k] += time_launches(fn, 10, stream)[1]
     check_device_error(ops)
     for k, (_, flops, extra) in launches.items():
         ms = statistics.mean(per[k])
@@ -484,6 +515,28 @@ def _variant_grouped(ops, wl, stream, dist_mod, peaks, steps, warm, dev):
                        "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
                                     "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"]}}, **extra)
         out[k]["launch_ms"] = launch_stats(per[k])
+    del A2, B2, D2, H
+    # rotating inputs: a second FC1 input set (activations and weights)
+    c3 = wl.grouped_case(seed=2005)
+    A3 = c3.A.to(dev)
+    B3 = [b.to(dev) for b in c3.Bs]
+    off3 = torch.from_numpy(c3.offsets).to(dev)
+    sets = [(a, bptrs, o), (A3.data_ptr(), [b.data_ptr() for b in B3], off3.data_ptr())]
+
+    def fc1_rot(i=0):
+        ai, bi, oi = sets[i % 2]
+        ops.grouped_gemm_bf16(ai, bi, d, oi, c.G, c.total, c.N, c.K, h)
+    for i in range(warm):
+        fc1_rot(i)
+    _, per_rot = time_launches(fc1_rot, max(10, steps // 2), stream)
+    check_device_error(ops)
+    ms = statistics.mean(per_rot)
+    tf = c.flops / (ms * 1e-3) / 1e12
+    out["grouped_fc1_32x4096x4096_rotating"] = {
+        "ms_per_launch": ms, "tflops": tf, "launch_ms": launch_stats(per_rot),
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tf / peaks["bf16_tflops"]},
+        "l2": "two input sets (2 x 1.34 GB, each with its own routing counts) taken in turn"}
     return out
 
 
@@ -495,20 +548,44 @@ def run_only(args):
     build.build()
     peaks, _ = load_peaks()
     stream = torch.cuda.current_stream()
-    res = measure_variants(ops, wl, stream, None, peaks, args.steps, only=args.only, warm=args.warmup)
+    res = measure_variants(ops, wl, stream, peaks, args.steps, only=args.only, warm=args.warmup)
     print(json.dumps(res), flush=True)
 
 
-def run_ours(args, rank, world, local):
+# --------------------------------------------------------------- ours -------
+
+def sustained_window(ops, launch, flops, stream, peaks, ms_hint):
+    """At least SUSTAINED_S seconds of back-to-back launches, with the clocks
+    sampled over them: the GPU reaches its power cap here."""
+    import torch
+    n = max(200, int(math.ceil(SUSTAINED_S * 1e3 / max(ms_hint, 1e-3))))
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    for _ in range(3):
+        launch()
+    total_ms, per = time_launches(launch, n, stream)
+    clocks = sampler.stop()
+    check_device_error(ops)
+    ms = total_ms / n
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"launches": n, "region_ms": total_ms, "ms_per_launch": ms, "tflops": tf,
+            "peak_sustained": peaks["bf16_tflops_sustained"],
+            "frac_of_sustained_peak": tf / peaks["bf16_tflops_sustained"],
+            "frac_of_burst_peak": tf / peaks["bf16_tflops"],
+            "launch_ms": dict(launch_stats(per), first_tenth_mean=statistics.mean(per[:n // 10]),
+                              last_tenth_mean=statistics.mean(per[-(n // 10):])),
+            "clocks": clocks}
+
+
+def run_ours(args):
     import torch
     from blackwell_tensor_core_gb300 import build, ops
     from blackwell_tensor_core_gb300 import workloads as wl
 
     if not torch.cuda.is_available():
         raise RuntimeError("bench.py needs a CUDA device (there is no CPU path)")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dist_mod = init_dist(world, "nccl")
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
     build.build()
     peaks, peak_src = load_peaks()
     stream = torch.cuda.current_stream(dev)
@@ -526,13 +603,12 @@ def run_ours(args, rank, world, local):
     sampler.start()
     for _ in range(3):  # keep the clocks up after the sampler's start-up
         launch()
-    total_ms, per = time_launches(launch, args.steps, stream, dist_mod)
+    total_ms, per = time_launches(launch, args.steps, stream)
     clocks = sampler.stop()
     check_device_error(ops)
-    total_ms = max_over_ranks(total_ms, dist_mod, dev)
 
     flops = case.flops
-    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    value = flops * args.steps / (total_ms * 1e-3) / 1e12
     mean_launch = statistics.mean(per)
     achieved = flops / (mean_launch * 1e-3) / 1e12
     # A timed region of a few hundred milliseconds runs before the power cap
@@ -544,19 +620,22 @@ def run_ours(args, rank, world, local):
     traffic = recorded_traffic()
     plan = ops.plan(case.M, case.N, case.K, sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
 
+    sustained = None
+    if not args.no_sustained:
+        sustained = sustained_window(ops, launch, flops, stream, peaks, mean_launch)
+
     # end to end through the host-buffer entry point (copies in the timed region)
     hA, hB = case.A.pin_memory(), case.B.pin_memory()
     hD = torch.empty((case.M, case.N), dtype=torch.bfloat16).pin_memory()
     e2e_steps = max(3, min(args.steps, 10))
 
-    def e2e_launch():
+    def e2e_launch(i=0):
         ops.gemm_bf16_host(hA, hB, hD, A, B, D, stream)
     e2e_launch()
     torch.cuda.synchronize()
-    e2e_ms, _ = time_launches(e2e_launch, e2e_steps, stream, dist_mod)
-    e2e_ms = max_over_ranks(e2e_ms, dist_mod, dev)
+    e2e_ms, _ = time_launches(e2e_launch, e2e_steps, stream)
     check_device_error(ops)
-    e2e = {"value": flops * e2e_steps * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+    e2e = {"value": flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
            "h2d_bytes_per_step": 2 * case.M * case.K + 2 * case.K * case.N,
            "d2h_bytes_per_step": 2 * case.M * case.N, "steps": e2e_steps,
            "api": "gemm_bf16_host (pinned host buffers, H2D + GEMM + D2H on one stream)"}
@@ -567,7 +646,7 @@ def run_ours(args, rank, world, local):
     if not args.no_variants:
         vs = ClockSampler(torch.cuda.current_device())
         vs.start()
-        variants = measure_variants(ops, wl, stream, dist_mod, peaks, min(args.steps, 200))
+        variants = measure_variants(ops, wl, stream, peaks, min(args.steps, 200))
         variant_clocks = vs.stop()
         # the variants run right after the long timed loop, at the power cap:
         # give their fractions of the sustained figure too
@@ -581,24 +660,24 @@ def run_ours(args, rank, world, local):
         context = cublas_context(ops, stream, dev)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         cpu = cpu_baseline(case)
+        if variants is not None:
+            # the oracle on each variant's own product (host cores only)
+            for name, v in measure_variant_oracles(wl).items():
+                if name in variants:
+                    variants[name].update(v)
 
-    if rank != 0:
-        return
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "gemm_8192x8192x8192_bf16in_fp32acc_bf16out", "M": case.M, "N": case.N,
-                   "K": case.K, "inputs": "U[-1,1], seed 1003, row-major A and B",
-                   "l2": "inputs larger than L2 (A+B = 256 MiB > 129 MB); no flush",
-                   "kernel": "%s, tile %dx%dx64, %d stages, grid %d" % (
-                       KERNEL_NAMES.get(plan.kernel, plan.kernel), plan.tile_m, plan.tile_n, plan.stages,
-                       plan.grid),
-                   "cluster": 2, "layout": "A [M,K] and B [K,N] row-major, D [M,N] row-major",
-                   "gpu": torch.cuda.get_device_name(dev), "toolchain": toolchain(),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": dict(CONFIG),
+        "build": {"kernel": "%s, tile %dx%dx64, %d stages, grid %d" % (
+                      KERNEL_NAMES.get(plan.kernel, plan.kernel), plan.tile_m, plan.tile_n, plan.stages,
+                      plan.grid),
+                  "cluster": 2, "gpu": torch.cuda.get_device_name(dev), "toolchain": toolchain(),
+                  "library": ops.version()},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": "%s %s (timed region %.0f ms)" % (peak_src, peak_key, total_ms),
@@ -606,6 +685,7 @@ def run_ours(args, rank, world, local):
                      "frac_of_sustained_peak": achieved / peaks["bf16_tflops_sustained"],
                      "algorithmic_flops_per_launch": flops,
                      "algorithmic_bytes_per_launch": 3 * 2 * case.M * case.N},
+        "sustained": sustained,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
@@ -620,29 +700,63 @@ def run_ours(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def measure_variant_oracles(wl):
+    """cpu_baseline objects of the variant workloads (oracle on host cores;
+    bounded samples, a few seconds each)."""
+    out = {}
+    c = wl.tile_case()
+    out["tile_256x256x512_fp32out"] = {"cpu_baseline": oracle_rate(wl.bits(c.A), wl.bits(c.B), 1.0)}
+    c = wl.small_m_case()
+    out["small_m_72x16384x7168"] = {"cpu_baseline": oracle_rate(wl.bits(c.A), wl.bits(c.B), 10.0)}
+    c = wl.square_case()
+    Ab, Bb = wl.bits(c.A), wl.bits(c.B)
+    out["square_4096"] = {"cpu_baseline": oracle_rate(Ab, Bb, 3.0),
+                          "cpu_baseline_one_core": oracle_rate(Ab, Bb, 3.0, threads=1)}
+    for name, case in (("grouped_fc1_32x4096x4096", wl.grouped_case()),
+                       ("grouped_fc2_32x4096x2048", wl.grouped_fc2_case())):
+        # one expert's rows against its own weight: the same arithmetic per row
+        g = int(max(range(case.G), key=lambda j: case.offsets[j + 1] - case.offsets[j]))
+        r0, r1 = int(case.offsets[g]), int(case.offsets[g + 1])
+        out[name] = {"cpu_baseline": oracle_rate(wl.bits(case.A[r0:r1]), wl.bits(case.Bs[g]), 3.0,
+                                                 what="expert %d: " % g)}
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3500)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sustained", action="store_true",
+                    help="skip the two-second back-to-back window (profiling runs)")
     ap.add_argument("--size", type=int, default=None,
                     help="square size of the timed GEMM (default 8192; smaller only for profiling)")
-    ap.add_argument("--only", choices=["tile", "small_m", "square", "grouped"], default=None,
+    ap.add_argument("--only", choices=["tile", "small_m", "square", "large_cold", "grouped"], default=None,
                     help="profiling aid: run only one variant workload, print its numbers")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    rank, world, local = dist_env()
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
+    rank, world = dist_env()
     if args.impl == "reference":
-        run_reference(args, rank)
+        # host cores only; under a multi-rank launcher rank 0 alone runs it
+        if rank == 0:
+            run_reference(args)
         return
+    if args.gpus != 1 or world != 1:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "impl": "ours", "n_gpus": max(args.gpus, world),
+                              "unavailable": ONE_GPU}), flush=True)
+        sys.stderr.write("bench.py: %s\n" % ONE_GPU)
+        sys.exit(2)
     if args.only:
         run_only(args)
         return
-    run_ours(args, rank, world, local)
+    run_ours(args)
 
 
 if __name__ == "__main__":

@@ -1,10 +1,17 @@
 """Build step for the CUDA library: compiles csrc/*.cu for sm_103a with nvcc
 (one translation unit per process, in parallel) and links libbwgemm.so into
 this package directory.  Run as ``python -m blackwell_tensor_core_gb300.build``
-or through ``__graft_entry__.build()``."""
+or through ``__graft_entry__.build()``.
+
+The library's ``bwg_version()`` ends with the hash of the code it was built
+from (every csrc file and the public header, comments removed); a library
+whose hash differs from the sources on disk, or that does not load on this
+machine, is rebuilt."""
 from __future__ import annotations
 
+import hashlib
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -15,6 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libbwgemm.so")
+HEADER = os.path.join(ROOT, "include", "bwgemm.h")
 SOURCES = ["api.cu", "gemm_tc.cu", "gemm_small_m.cu", "probes.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -26,12 +34,49 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA library cannot be built")
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source with comments and blank space removed, so that a hash
+    of it changes with the code, not with its comments."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def library_files() -> list:
+    """Every file the library is compiled from: csrc/* and the public header."""
+    names = sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h")))
+    return [os.path.join(CSRC, f) for f in names] + [HEADER]
+
+
+def source_hash(paths=None) -> str:
+    """16 hex digits of SHA-256 over the code-only text of `paths` (default:
+    every library source), in order."""
+    h = hashlib.sha256()
+    for path in (paths if paths is not None else library_files()):
+        with open(path, encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
+    return h.hexdigest()[:16]
+
+
+def built_version(path: str = LIB):
+    """bwg_version() of the library at `path`, read in a child process (so that
+    this process does not keep a stale copy loaded); None if it cannot load."""
+    if not os.path.exists(path):
+        return None
+    code = ("import ctypes,sys; L=ctypes.CDLL(sys.argv[1]); L.bwg_version.restype=ctypes.c_char_p; "
+            "print(L.bwg_version().decode())")
+    try:
+        r = subprocess.run([sys.executable, "-c", code, path], capture_output=True, text=True, timeout=60)
+    except (OSError, subprocess.SubprocessError):
+        return None
+    return r.stdout.strip() if r.returncode == 0 else None
+
+
 def _up_to_date() -> bool:
-    if not os.path.exists(LIB):
-        return False
-    t = os.path.getmtime(LIB)
-    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "bwgemm.h")]
-    return all(os.path.getmtime(d) <= t for d in deps)
+    """The library exists, loads on this machine and was built from the
+    sources as they are now (its version string carries their hash)."""
+    v = built_version()
+    return v is not None and v.endswith("source " + source_hash())
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -40,7 +85,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
     cc = nvcc()
     flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
-                    "-I" + os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]
+                    "-I" + os.path.join(ROOT, "include"), "--expt-relaxed-constexpr",
+                    '-DBWG_SOURCE_HASH="%s"' % source_hash()]
     if os.environ.get("BWG_PTXAS_VERBOSE"):
         flags += ["-Xptxas", "-v"]
 

@@ -92,34 +92,63 @@ struct MapKeyHash {
 };
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
-// Stream-K workspace of the small-M kernel, one per (device, stream): FP32
-// partial accumulators and per-tile arrival counters.  Counters are zeroed
-// when the buffer is made and every call leaves them at zero again.  A
-// workspace is reused only by calls on its own stream, so calls on one stream
-// are ordered; calls on different streams use different workspaces.
+// Stream-K workspace of the small-M kernel (and of the opt-in dense stream-K
+// last wave), one per (device, stream): FP32 partial accumulators and
+// per-tile arrival counters.  Counters are zeroed when the buffer is made and
+// every call leaves them at zero again.  A workspace is reused only by calls
+// on its own stream, so calls on one stream are ordered; calls on different
+// streams use different workspaces.  Streams are told apart by the runtime's
+// stream id, not by the handle: the per-thread default stream has one handle
+// but a different stream (and id) in each host thread, and a handle of a
+// destroyed stream can come back for a new one.  The buffers are allocated
+// (cudaMalloc) on the first call that needs them on a stream and grown when a
+// later call needs more; they live until the process exits.  Growing them
+// while the stream is being captured into a graph is refused
+// (BWG_ERR_UNSUPPORTED): make one eager call of the largest shape first.
 struct Workspace {
   float* ws = nullptr;
   int* counters = nullptr;
   size_t ws_bytes = 0;
   int n_counters = 0;
 };
-std::unordered_map<unsigned long long, Workspace> g_workspaces;
+struct WorkspaceKey {
+  int dev;
+  unsigned long long stream_id;
+  bool operator==(const WorkspaceKey& o) const { return dev == o.dev && stream_id == o.stream_id; }
+};
+struct WorkspaceKeyHash {
+  size_t operator()(const WorkspaceKey& k) const {
+    return static_cast<size_t>((k.stream_id * 1099511628211ull) ^ static_cast<unsigned long long>(k.dev));
+  }
+};
+std::unordered_map<WorkspaceKey, Workspace, WorkspaceKeyHash> g_workspaces;
 
 bwg_status get_workspace(cudaStream_t stream, size_t ws_bytes, int n_counters, Workspace* out) {
   int dev = 0;
-  cudaGetDevice(&dev);
-  const unsigned long long key =
-      (static_cast<unsigned long long>(dev) << 56) ^ reinterpret_cast<uintptr_t>(stream);
+  unsigned long long sid = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaStreamGetId(stream, &sid) != cudaSuccess) {
+    cudaGetLastError();
+    return BWG_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lock(g_mu);
-  Workspace& w = g_workspaces[key];
+  Workspace& w = g_workspaces[WorkspaceKey{dev, sid}];
   if (w.ws_bytes < ws_bytes || w.n_counters < n_counters) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+      cudaGetLastError();
+      return BWG_ERR_CUDA;
+    }
+    if (cap != cudaStreamCaptureStatusNone) return BWG_ERR_UNSUPPORTED;
     // grow to cover both the old and the new request, so that alternating
     // shapes settle on one buffer instead of reallocating every call
     const size_t wb = std::max(ws_bytes, w.ws_bytes);
     const int nc = std::max(n_counters, w.n_counters);
     if (w.ws != nullptr || w.counters != nullptr) {
       // the old buffers may still be in use by work queued on this stream
-      if (cudaStreamSynchronize(stream) != cudaSuccess) return BWG_ERR_CUDA;
+      if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return BWG_ERR_CUDA;
+      }
       cudaFree(w.ws);
       cudaFree(w.counters);
       w = Workspace();
@@ -140,14 +169,13 @@ bwg_status get_workspace(cudaStream_t stream, size_t ws_bytes, int n_counters, W
   return BWG_OK;
 }
 
-// Most CTAs that share one tile under the stream-K split.
 // Zero every stream-K arrival counter of this device (after a timeout).
 bwg_status clear_workspace_counters() {
   int dev = 0;
   cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lock(g_mu);
   for (auto& kv : g_workspaces) {
-    if (static_cast<int>(kv.first >> 56) != dev || kv.second.counters == nullptr) continue;
+    if (kv.first.dev != dev || kv.second.counters == nullptr) continue;
     if (cudaMemset(kv.second.counters, 0, static_cast<size_t>(kv.second.n_counters) * sizeof(int)) !=
         cudaSuccess)
       return BWG_ERR_CUDA;
@@ -155,6 +183,7 @@ bwg_status clear_workspace_counters() {
   return BWG_OK;
 }
 
+// Most CTAs that share one tile under the stream-K split.
 int streamk_max_sharers(int tiles, int kb, int grid) {
   const long long W = static_cast<long long>(tiles) * kb;
   int most = 1;
@@ -312,7 +341,8 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
     // 128 columns per tile by default: narrower strides start B's boxes off a
     // 128-byte boundary, which measured slower than leaving SMs idle.
     int tn = 128;
-    if (const char* v = std::getenv("BWG_SMALL_M_TILE_N")) {
+    const char* tn_env = force_streamk ? nullptr : std::getenv("BWG_SMALL_M_TILE_N");
+    if (const char* v = tn_env) {
       const int f = std::atoi(v);
       if (f >= 16 && f <= 128 && f % 16 == 0) tn = f;
     }
@@ -670,6 +700,19 @@ CUtensorMapDataType out_map_dtype(int out_dtype) {
   return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 }
 
+// Whether p points into device memory of the current device (allocated on
+// it with cudaMalloc or a pool on it).
+bool local_device_memory(const void* p) {
+  int dev = 0;
+  cudaPointerAttributes a;
+  std::memset(&a, 0, sizeof(a));
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
 bwg_status launch_status(cudaError_t e) {
   if (e == cudaSuccess) return BWG_OK;
   cudaGetLastError();
@@ -739,6 +782,13 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
     }
     return launch_status(launch_small_m(p, pl.grid, pl.smem_total, stream));
   }
+  // The multicast kernel's loads land in the shared memory of two CTA pairs
+  // at once; it may read only memory that this GPU owns.  Anything else (host
+  // memory, another GPU's memory, managed memory) is refused before any
+  // descriptor is made or any kernel launched.
+  if (pl.kernel == BWG_KERNEL_2CTA_MC &&
+      (!local_device_memory(A) || !local_device_memory(B)))
+    return BWG_ERR_INVALID_ARG;
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   const uint32_t d_box_inner = out_dtype == BWG_OUT_FP32 ? 32 : 64;
@@ -1158,15 +1208,24 @@ bwg_status gemm_bf16_host(const void* A_host, const void* B_host, void* D_host, 
     e = cudaStreamWaitEvent(us, st->ev_in[c], 0);
     if (e != cudaSuccess) break;
     s = run_dense(false, a_at(dA, r0), dB, d_at(dD, r0), rc, N, K, K, N, N, out_dtype, us);
-    if (s != BWG_OK) return s;
+    if (s != BWG_OK) break;
     e = cudaEventRecord(st->ev_out[c], us);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st->d2h, st->ev_out[c], 0);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(d_at(D_host, r0), d_at(dD, r0), static_cast<size_t>(rc) * N * oe,
                           cudaMemcpyDeviceToHost, st->d2h);
   }
+  if (s != BWG_OK || e != cudaSuccess) {
+    // Copies of this call may already be queued on the copy streams: let them
+    // finish before returning, so that the caller may free or reuse its host
+    // buffers as soon as it sees the error.
+    cudaStreamSynchronize(st->h2d);
+    cudaStreamSynchronize(st->d2h);
+    cudaGetLastError();
+    return s != BWG_OK ? s : fail(e);
+  }
   // the caller's stream finishes after the last copy back
-  if (e == cudaSuccess) e = cudaEventRecord(st->ev_done, st->d2h);
+  e = cudaEventRecord(st->ev_done, st->d2h);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(us, st->ev_done, 0);
   return fail(e);
 }
@@ -1328,6 +1387,11 @@ int bwg_grouped_swap_rows(int m0, int row_end, int tile_m) {
   return grouped_swap_rows(m0, row_end, tile_m);
 }
 
-const char* bwg_version(void) { return "bwgemm 0.1 (sm_103a)"; }
+#ifndef BWG_SOURCE_HASH
+#define BWG_SOURCE_HASH "unknown"
+#endif
+// The build passes the hash of the library's sources (code only, comments
+// and blank space removed), so that a loaded binary can be matched to them.
+const char* bwg_version(void) { return "bwgemm 0.2 (sm_103a) source " BWG_SOURCE_HASH; }
 
 }  // extern "C"

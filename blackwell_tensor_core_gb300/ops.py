@@ -25,7 +25,8 @@ _OUT_CODES = {torch.bfloat16: OUT_BF16, torch.float32: OUT_FP32, torch.float16: 
 KERNEL_NONE, KERNEL_ZERO, KERNEL_1CTA, KERNEL_2CTA, KERNEL_SMALL_M, KERNEL_2CTA_MC, KERNEL_2CTA_2C = range(7)
 
 STATUS_NAMES = {0: "BWG_OK", 1: "BWG_ERR_INVALID_ARG", 2: "BWG_ERR_ALIGNMENT",
-                3: "BWG_ERR_UNSUPPORTED", 4: "BWG_ERR_CUDA", 5: "BWG_ERR_TIMEOUT"}
+                3: "BWG_ERR_UNSUPPORTED", 4: "BWG_ERR_CUDA", 5: "BWG_ERR_TIMEOUT",
+                6: "BWG_ERR_SCRATCH_LIMIT"}
 
 _lock = threading.Lock()
 _lib = None
@@ -124,6 +125,11 @@ def lib() -> ctypes.CDLL:
             L.bwg_version.restype = ctypes.c_char_p
             _lib = L
     return _lib
+
+
+def version() -> str:
+    """bwg_version(): library version and the hash of the sources it was built from."""
+    return lib().bwg_version().decode()
 
 
 def status_string(status: int) -> str:

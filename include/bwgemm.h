@@ -61,7 +61,18 @@ typedef enum { BWG_OUT_BF16 = 0, BWG_OUT_FP32 = 1, BWG_OUT_FP16 = 2 } bwg_out_dt
  *   sum their partials in shared memory; with more tiles than SMs and a ragged
  *   last wave they share k-blocks stream-K style through a device workspace
  *   that the library allocates (cudaMalloc) on the first such call on a
- *   stream and keeps for later calls on that stream.
+ *   stream and keeps, until the process exits, for later calls on that
+ *   stream (streams are told apart by their runtime id, so the per-thread
+ *   default stream of each host thread has its own).  A call that would have
+ *   to grow that workspace while its stream is being captured into a CUDA
+ *   graph returns BWG_ERR_UNSUPPORTED: make one eager call of the largest
+ *   shape on the stream first.  Callers that must never see the library
+ *   allocate can use gemm_bf16_small_m_noalloc below.
+ *   The library also holds a TMA-multicast variant of the pair kernel (two
+ *   CTA pairs receive every box of B), selected only by the environment
+ *   override BWG_FORCE_KERNEL=2cta_mc; it reads only device memory of the
+ *   current GPU, and operands anywhere else (host, another GPU, managed
+ *   memory) make the call return BWG_ERR_INVALID_ARG before any launch.
  */
 bwg_status gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K, int lda, int ldb,
                      int ldd, int out_dtype, void* stream);
@@ -159,9 +170,15 @@ bwg_status grouped_gemm_swiglu_fp16_nt(const void* A, const void* const* B, void
  * rules) with the stream-K small-M kernel, keeping that kernel's partial sums
  * and per-tile counters in one fixed 32 MiB device array inside the library
  * instead of an allocated workspace:
- *   - the array exists on every GPU that loads the library, until exit;
- *   - the first call on a device looks up the array's device address (a
- *     runtime symbol lookup); make that first call before any stream capture;
+ *   - the array is part of the library's device code: it takes device
+ *     memory on a GPU once that code is loaded there, which (with the CUDA
+ *     runtime's default lazy loading) is the first call of any bwgemm entry
+ *     point on that device, and keeps it until the process exits.  A caller
+ *     that hands all free device memory to its own pool should therefore
+ *     make that first call before reserving the pool;
+ *   - the first call of this entry point on a device looks up the array's
+ *     device address (a runtime symbol lookup, with that device current) and
+ *     keeps it; make that first call before any stream capture;
  *   - every call shares the array and leaves its contents behind; each call
  *     clears the tile counters it needs (cudaMemsetAsync on `stream`), so
  *     calls on one stream are safe, but calls whose GPU work overlaps (other
@@ -190,7 +207,9 @@ bwg_status gemm_bf16_small_m_noalloc(const void* A, const void* B, void* D, int 
  * synchronises `stream` before reading D_host.  The internal streams and
  * events are made on a device's first call and kept; calls from several
  * host threads on one device are serialised while they enqueue.  The
- * library allocates no device memory.
+ * library allocates no device memory.  A call that fails after it has queued
+ * copies waits for those copies before it returns its error, so the host
+ * buffers may be freed or reused as soon as it returns.
  */
 bwg_status gemm_bf16_host(const void* A_host, const void* B_host, void* D_host, int M, int N, int K,
                           int out_dtype, void* dA, void* dB, void* dD, void* stream);
@@ -421,7 +440,10 @@ void bwg_streamk_tile_workers(int t, int kb, long long W, int C, int* first, int
  * 128 go on the MMA's N), else 0. */
 int bwg_grouped_swap_rows(int m0, int row_end, int tile_m);
 
-/* Library version string. */
+/* Library version string (static): "bwgemm <version> (sm_103a) source <hash>",
+ * where <hash> is 16 hex digits of SHA-256 over the code of the sources the
+ * library was built from (every csrc file and this header, comments and blank
+ * space removed), so that a loaded binary can be matched to its sources. */
 const char* bwg_version(void);
 
 #ifdef __cplusplus

@@ -90,6 +90,8 @@ def _load():
             lib.oracle_round_fp16.restype = ctypes.c_uint16
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+            lib.oracle_set_num_threads.restype = None
             _lib = lib
     return _lib
 
@@ -107,6 +109,11 @@ def _ptr(a: np.ndarray, ctype):
 def num_threads() -> int:
     """OpenMP threads the oracle runs on."""
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Run later calls on `n` OpenMP threads (timing aid; results do not change)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def decode(bits: np.ndarray, dtype: str = "bf16") -> np.ndarray:

@@ -209,3 +209,13 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Number of threads later calls run on (at least 1).  Timing aid: the
+ * arithmetic is the same on any number of threads. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : 1);
+#else
+    (void)n;
+#endif
+}

@@ -141,6 +141,35 @@ def test_bad_arguments_return_status():
     assert e.value.status == 2
 
 
+def test_multicast_kernel_reads_only_this_gpus_memory():
+    """The multicast kernel (two CTA pairs receiving each B box) may read only
+    device memory of the GPU it runs on: operands in pinned host memory are
+    refused with BWG_ERR_INVALID_ARG before any descriptor or launch, and the
+    output is left untouched; the same call on device operands runs."""
+    from blackwell_tensor_core_gb300 import ops
+    from gpu_util import forced_kernel
+    g = wl.generator(2300)
+    M, N, K = 512, 512, 256
+    A = wl.randint_matrix(M, K, -2, 2, g)
+    B = wl.randint_matrix(K, N, -2, 2, g)
+    Ad, Bd = A.cuda(), B.cuda()
+    Ah, Bh = A.pin_memory(), B.pin_memory()
+    D = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
+    h = torch.cuda.current_stream().cuda_stream
+    L = ops.lib()
+    with forced_kernel("2cta_mc"):
+        for a, b in ((Ad, Bh), (Ah, Bd), (Ah, Bh)):
+            st = L.gemm_bf16(a.data_ptr(), b.data_ptr(), D.data_ptr(), M, N, K, K, N, N, wl.OUT_FP32, h)
+            assert st == 1
+        torch.cuda.synchronize()
+        assert bool((D == 7.0).all())
+        assert L.gemm_bf16(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K, K, N, N, wl.OUT_FP32, h) == 0
+    torch.cuda.synchronize()
+    assert ops.last_device_error()[0] == 0
+    Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+    assert np.array_equal(D.cpu().double().numpy(), Dref)
+
+
 # ------------------------------------------- full-size method workloads ----
 
 def _sample_indices(M, N, n, seed, tile_m=256, tile_n=256):
