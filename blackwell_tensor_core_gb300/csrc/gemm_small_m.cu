@@ -275,56 +275,71 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
     if (lane == 0) producer.issue(0x7FFFFFFF, &aborted);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      int s = 0;
-      uint32_t ph = 0;
-      int acc = 0;
-      uint32_t acc_ph = 0;
-      int t, kb0, kb1;
-      for (int i = 0; !aborted && segs.get(i, &t, &kb0, &kb1); ++i) {
-        if (!mbar_wait(acc_empty_bar(acc), acc_ph ^ 1u, p.timeout_ns)) {
-          record_fault_small(p.err, 1, 3, acc, acc_ph ^ 1u);
+    // MMA issuer.  The whole warp walks the loop, so that stage indices and
+    // descriptors stay warp-uniform, and one elected lane issues the MMAs and
+    // commits.  (Issued from a single lane of a diverged warp, the four small
+    // MMAs of a stage took longer than the stage's bytes take to arrive, and
+    // that, not memory, set the kernel's streaming rate.)  Two stages filled
+    // by one load are issued after one wait: their bytes complete on the
+    // first stage's barrier.
+    int s = 0;
+    uint32_t ph = 0;
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    int t, kb0, kb1;
+    // MMA A = B^T tile (MN-major, two 64-channel boxes 8 KiB apart, the next
+    // 16 K values 16 rows = 2 KiB further); MMA B = A tile (K-major, 128-byte
+    // rows, 8-row groups 1 KiB apart, the next 16 K values 32 bytes along each
+    // row).  B stored as [N, K]: the MMA A operand is K-major like the B one.
+    const uint32_t a_lbo = p.b_kmajor ? 16u : kBtChunkBytes;
+    const uint32_t a_step = p.b_kmajor ? 32u : 2048u;
+    for (int i = 0; !aborted && segs.get(i, &t, &kb0, &kb1); ++i) {
+      if (!warp_wait_all(acc_empty_bar(acc), acc_ph ^ 1u, p.timeout_ns)) {
+        if (lane == 0) record_fault_small(p.err, 1, 3, acc, acc_ph ^ 1u);
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * 256u;
+      for (int kb = kb0; kb < kb1;) {
+        // the producer's choice for this stage: one load for stages s, s+1
+        const int n = (p.pair_loads && (s & 1) == 0 && s + 1 < S && kb + 2 <= kb1) ? 2 : 1;
+        if (!warp_wait_all(full_bar(s), ph, p.timeout_ns)) {
+          if (lane == 0) record_fault_small(p.err, 1, 0, s, ph);
           aborted = true;
           break;
         }
+        if (trace != nullptr && lane == 0 && i == 0 && kb == kb0) trace[1] = globaltimer_ns();
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * 256u;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(full_bar(s), ph, p.timeout_ns)) {
-            record_fault_small(p.err, 1, 0, s, ph);
-            aborted = true;
-            break;
-          }
-          if (trace != nullptr && i == 0 && kb == kb0) trace[1] = globaltimer_ns();
-          tc_fence_after();
-          // MMA A = B^T tile (MN-major, two 64-channel boxes 8 KiB apart),
-          // MMA B = A tile (K-major, 128-byte rows, 8-row groups 1 KiB apart).
-          // (B stored as [N, K]: the MMA A operand is K-major, 8-row groups
-          // 1 KiB apart, the next 16 K values 32 bytes along each row.)
-          const uint64_t a_desc = make_smem_desc(smem_bt + s * kBtStageBytes,
-                                                 p.b_kmajor ? 16u : kBtChunkBytes, 1024, kSwizzle128B);
-          const uint32_t a_step = p.b_kmajor ? 32u : 2048u;
-          const uint64_t b_desc = make_smem_desc(smem_at + s * at_stage_bytes, 16, 1024, kSwizzle128B);
+        for (int j = 0; j < n; ++j) {
+          const uint32_t sj = static_cast<uint32_t>(s + j);
+          const uint64_t a_desc = make_smem_desc(smem_bt + sj * kBtStageBytes, a_lbo, 1024, kSwizzle128B);
+          const uint64_t b_desc = make_smem_desc(smem_at + sj * at_stage_bytes, 16, 1024, kSwizzle128B);
+          const bool first = kb + j == kb0;
+          if (elect_one()) {
 #pragma unroll
-          for (uint32_t kk = 0; kk < kBK / 16; ++kk)
-            mma_f16<1>(d_tmem, a_desc + ((kk * a_step) >> 4), b_desc + ((kk * 32u) >> 4), p.idesc,
-                       (kb > kb0 || kk > 0) ? 1u : 0u);
-          mma_commit_1cta(empty_bar(s));
-          if (++s == S) {
-            s = 0;
-            ph ^= 1u;
+            for (uint32_t kk = 0; kk < kBK / 16; ++kk)
+              mma_f16<1>(d_tmem, a_desc + ((kk * a_step) >> 4), b_desc + ((kk * 32u) >> 4), p.idesc,
+                         (!first || kk > 0) ? 1u : 0u);
+            mma_commit_1cta(empty_bar(static_cast<int>(sj)));
           }
+          __syncwarp();
         }
-        if (aborted) break;
-        mma_commit_1cta(acc_full_bar(acc));
-        if (trace != nullptr) trace[2] = globaltimer_ns();
-        if (++acc == 2) {
-          acc = 0;
-          acc_ph ^= 1u;
+        kb += n;
+        if ((s += n) == S) {
+          s = 0;
+          ph ^= 1u;
         }
       }
+      if (aborted) break;
+      if (elect_one()) mma_commit_1cta(acc_full_bar(acc));
+      __syncwarp();
+      if (trace != nullptr && lane == 0) trace[2] = globaltimer_ns();
+      if (++acc == 2) {
+        acc = 0;
+        acc_ph ^= 1u;
+      }
     }
-    __syncwarp();
   } else {
     // Epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = output columns.
     const uint32_t q = warp & 3u;

@@ -491,7 +491,9 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
     }
     __syncwarp();
   } else if (warp >= 1 && warp <= static_cast<uint32_t>(NC)) {
-    // ---- MMA issuer: one thread of CTA 0 drives the tensor cores -----------
+    // ---- MMA issuer: one warp of CTA 0 drives the tensor cores -------------
+    // The whole warp walks the loop (stage indices and descriptors stay
+    // warp-uniform) and one elected lane issues the MMAs and commits.
     // With two consumers, warp 1 + c issues consumer c's MMAs (its A block,
     // the shared B stage) into TMEM columns [256c, 256c + 256).
     // Commit masks: the stage-empty signal must reach every CTA whose shared
@@ -500,14 +502,14 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
     const uint16_t empty_mask = static_cast<uint16_t>(MC == 2 ? 0xF : 0x3);
     const uint16_t acc_mask = static_cast<uint16_t>(0x3u << (2 * pair));
     const int cons = static_cast<int>(warp) - 1;  // consumer of this warp
-    if (rank == 0 && lane == 0) {
+    if (rank == 0) {
       int s = 0;
       uint32_t ph = 0;
       int acc = NC == 1 ? 0 : cons;  // accumulator slot: alternating, or the consumer's own
       uint32_t acc_ph = 0;
       uint32_t k = 0;
       for (int t = first; DYN ? t >= 0 : t < total;
-           t = next_unit(t, k, kRoleMma, /*arm=*/false, /*warp_wide=*/false)) {
+           t = next_unit(t, k, kRoleMma, /*arm=*/false, /*warp_wide=*/true)) {
         if (t >= total) continue;
         const Tile tl = sched.at(t);
         if (tl.width == 0) continue;
@@ -516,15 +518,18 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
           // stage-empty barrier counts every consumer), after the stage's
           // full phase so the commit lands in the right phase.
           for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
-            if (!mbar_wait(full_bar(s), ph, p.timeout_ns)) {
-              record_fault(p.err, kFaultTimeout, kRoleMma, kBarFull, s, ph);
+            if (!warp_wait(full_bar(s), ph, p.timeout_ns)) {
+              if (lane == 0) record_fault(p.err, kFaultTimeout, kRoleMma, kBarFull, s, ph);
               aborted = true;
               break;
             }
-            if constexpr (CG == 2)
-              mma_commit_pair_mc(empty_bar(s), empty_mask);
-            else
-              mma_commit_1cta(empty_bar(s));
+            if (elect_one()) {
+              if constexpr (CG == 2)
+                mma_commit_pair_mc(empty_bar(s), empty_mask);
+              else
+                mma_commit_1cta(empty_bar(s));
+            }
+            __syncwarp();
             if (++s == S) {
               s = 0;
               ph ^= 1u;
@@ -533,8 +538,8 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
           if (aborted) break;
           continue;
         }
-        if (!mbar_wait(acc_empty_bar(acc), acc_ph ^ 1u, p.timeout_ns)) {
-          record_fault(p.err, kFaultTimeout, kRoleMma, kBarAccEmpty, acc, acc_ph ^ 1u);
+        if (!warp_wait(acc_empty_bar(acc), acc_ph ^ 1u, p.timeout_ns)) {
+          if (lane == 0) record_fault(p.err, kFaultTimeout, kRoleMma, kBarAccEmpty, acc, acc_ph ^ 1u);
           aborted = true;
           break;
         }
@@ -547,8 +552,8 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
             swapped ? idesc_with_n(p.idesc_swap, static_cast<uint32_t>((tl.swap_rows + 15) & ~15))
                     : idesc_with_n(p.idesc, static_cast<uint32_t>(tl.width));
         for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
-          if (!mbar_wait(full_bar(s), ph, p.timeout_ns)) {
-            record_fault(p.err, kFaultTimeout, kRoleMma, kBarFull, s, ph);
+          if (!warp_wait(full_bar(s), ph, p.timeout_ns)) {
+            if (lane == 0) record_fault(p.err, kFaultTimeout, kRoleMma, kBarFull, s, ph);
             aborted = true;
             break;
           }
@@ -562,29 +567,35 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
           const uint64_t b_desc = make_smem_desc(smem_b + s * kBStageBytes, bk ? 16u : kBChunkBytes,
                                                  1024, kSwizzle128B);
           const uint32_t b_step = bk ? 32u : 2048u;
+          if (elect_one()) {
 #pragma unroll
-          for (uint32_t kk = 0; kk < kBK / 16; ++kk) {
-            // K-major A: the next 16 K values are 32 bytes further along each
-            // 128-byte row.
-            const uint64_t ad = a_desc + ((kk * 32u) >> 4);
-            const uint64_t bd = b_desc + ((kk * b_step) >> 4);
-            mma_f16<CG>(d_tmem, swapped ? bd : ad, swapped ? ad : bd, idesc,
-                        (kb != tl.kb0 || kk != 0) ? 1u : 0u);
+            for (uint32_t kk = 0; kk < kBK / 16; ++kk) {
+              // K-major A: the next 16 K values are 32 bytes further along
+              // each 128-byte row.
+              const uint64_t ad = a_desc + ((kk * 32u) >> 4);
+              const uint64_t bd = b_desc + ((kk * b_step) >> 4);
+              mma_f16<CG>(d_tmem, swapped ? bd : ad, swapped ? ad : bd, idesc,
+                          (kb != tl.kb0 || kk != 0) ? 1u : 0u);
+            }
+            if constexpr (CG == 2)
+              mma_commit_pair_mc(empty_bar(s), empty_mask);
+            else
+              mma_commit_1cta(empty_bar(s));
           }
-          if constexpr (CG == 2)
-            mma_commit_pair_mc(empty_bar(s), empty_mask);
-          else
-            mma_commit_1cta(empty_bar(s));
+          __syncwarp();
           if (++s == S) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (aborted) break;
-        if constexpr (CG == 2)
-          mma_commit_pair_mc(acc_full_bar(acc), acc_mask);
-        else
-          mma_commit_1cta(acc_full_bar(acc));
+        if (elect_one()) {
+          if constexpr (CG == 2)
+            mma_commit_pair_mc(acc_full_bar(acc), acc_mask);
+          else
+            mma_commit_1cta(acc_full_bar(acc));
+        }
+        __syncwarp();
         if constexpr (NC == 1) {
           if (++acc == 2) {
             acc = 0;

@@ -129,6 +129,26 @@ BWG_DEV bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   }
 }
 
+// Warp-wide bounded wait: every lane waits, and the result is true only if
+// all lanes saw the phase complete.
+BWG_DEV bool warp_wait_all(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const bool ok = mbar_wait(bar, parity, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// True in one lane of the (converged) warp.  Issuing tcgen05 operations from
+// an elected lane of a warp that runs the loop together, rather than from a
+// single lane of a diverged warp, keeps their operands warp-uniform.
+BWG_DEV bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred)
+      :
+      : "memory");
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------- math ----
 
 // Hardware approximate reciprocal (flushes subnormal inputs and results to
