@@ -769,6 +769,11 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
     p.split = pl.split;
     p.b_kmajor = b_kmajor ? 1 : 0;
     p.staging_in_ring = pl.staging_in_ring;
+    // B^T streams through L2 as evict-first (whole tiles and stream-K; the
+    // cluster split measured 5% slower with it); BWG_SMALL_M_L2HINT
+    // overrides (bit 1: B^T evict-first, bit 0: A evict-last).
+    p.l2hint = pl.split > 1 ? 0 : 2;
+    if (const char* v = std::getenv("BWG_SMALL_M_L2HINT")) p.l2hint = std::atoi(v) & 3;
     p.d = D;
     p.ldd = ldd;
     p.trace = g_trace.load();
@@ -1056,6 +1061,7 @@ bwg_status run_small_m_noalloc(const void* A, const void* B, void* D, int M, int
   p.idesc = pl.idesc;
   p.tx_extra = g_tx_extra.load();
   p.streamk = 1;
+  p.l2hint = 2;  // B^T evict-first, as in gemm_bf16
   p.ws_slots = slots;
   p.ws_counters = static_cast<int*>(scratch);
   p.ws = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + kNoAllocCounterBytes);

@@ -185,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
     const Segments& segs;
     uint32_t smem_bt, smem_at, at_stage_bytes, bar0, tx;
     int S, i = 0, kb = 0, kb1 = 0, n0 = 0, s = 0;
+    uint64_t pol_a = 0, pol_b = 0;  // L2 policies of the A and B^T loads
     uint32_t ph = 0;
     bool have = false, done = false;
     __device__ void issue(int limit, bool* aborted) {
@@ -222,10 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
         if (pair) {
           mbar_arrive_expect_tx(full, 2u * (tx - p.tx_extra) + p.tx_extra);
           if (p.b_kmajor)
-            tma_load_3d(sbt, &p.map_bt2, full, 0, n0, kb);
+            tma_load_3d_hint(sbt, &p.map_bt2, full, 0, n0, kb, pol_b);
           else
-            tma_load_4d(sbt, &p.map_bt2, full, 0, 0, n0 >> 6, kb);
-          tma_load_3d(sat, &p.map_at2, full, 0, 0, kb);
+            tma_load_4d_hint(sbt, &p.map_bt2, full, 0, 0, n0 >> 6, kb, pol_b);
+          tma_load_3d_hint(sat, &p.map_at2, full, 0, 0, kb, pol_a);
           mbar_arrive_local(full + 8u);
           if ((s += 2) == S) {
             s = 0;
@@ -240,14 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
         // (channel, k) or (channel in group, k, group), B stored as [N, K]
         // (k, channel)
         if (p.b_kmajor) {
-          tma_load_2d(sbt, &p.map_bt, full, k0, n0);
+          tma_load_2d_hint(sbt, &p.map_bt, full, k0, n0, pol_b);
         } else if (p.bt_boxes == 1) {
-          tma_load_3d(sbt, &p.map_bt, full, 0, k0, n0 >> 6);
+          tma_load_3d_hint(sbt, &p.map_bt, full, 0, k0, n0 >> 6, pol_b);
         } else {
-          tma_load_2d(sbt, &p.map_bt, full, n0, k0);
-          tma_load_2d(sbt + kBtChunkBytes, &p.map_bt, full, n0 + 64, k0);
+          tma_load_2d_hint(sbt, &p.map_bt, full, n0, k0, pol_b);
+          tma_load_2d_hint(sbt + kBtChunkBytes, &p.map_bt, full, n0 + 64, k0, pol_b);
         }
-        tma_load_2d(sat, &p.map_at, full, k0, 0);
+        tma_load_2d_hint(sat, &p.map_at, full, k0, 0, pol_a);
         if (++s == S) {
           s = 0;
           ph ^= 1u;
@@ -257,6 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
       }
     }
   } producer{p, segs, smem_bt, smem_at, at_stage_bytes, smem_bar, stage_bytes + p.tx_extra, S};
+  // B streams through once, so its loads go in as first to evict: the B
+  // lines then do not push A (which every CTA reads) and D out of L2.
+  // Measured on GB300 at 72x16384x7168: 43.0 -> 40.9 us; at 128 rows
+  // 49.1 -> 40.9 us.  A keeps the normal policy (evict-last gained nothing).
+  if (threadIdx.x == 0) {
+    producer.pol_b = (p.l2hint & 2) ? l2_policy_evict_first() : l2_policy_evict_normal();
+    producer.pol_a = (p.l2hint & 1) ? l2_policy_evict_last() : l2_policy_evict_normal();
+  }
   if (threadIdx.x == 0) producer.issue(S, &aborted);
   if (warp == 1) {
     tmem_alloc<1>(tmem_slot, kTmemCols);

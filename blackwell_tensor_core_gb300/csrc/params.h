@@ -119,6 +119,8 @@ struct SmallMParams {
   int bt_boxes;         // loads per single stage of B^T (1 or 2), see map_bt
   int pair_loads;       // 1: fill stages s, s+1 (s even) with map_bt2 / map_at2 where two
                         // k-blocks of the segment remain
+  int l2hint;           // L2 policies: bit 1 loads B^T evict-first (the default), bit 0
+                        // loads A evict-last; evict-normal where a bit is clear
   void* d;            // D (split mode stores its rows directly)
   long long ldd;      // D's leading dimension, elements
   // Optional trace (nullptr: off): per CTA eight global-timer stamps (ns),
