@@ -104,7 +104,8 @@ std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 // (cudaMalloc) on the first call that needs them on a stream and grown when a
 // later call needs more; they live until the process exits.  Growing them
 // while the stream is being captured into a graph is refused
-// (BWG_ERR_UNSUPPORTED): make one eager call of the largest shape first.
+// (BWG_ERR_UNSUPPORTED): make one eager call of the largest shape first, on
+// the same stream and from the same host thread.
 struct Workspace {
   float* ws = nullptr;
   int* counters = nullptr;
@@ -123,22 +124,37 @@ struct WorkspaceKeyHash {
 };
 std::unordered_map<WorkspaceKey, Workspace, WorkspaceKeyHash> g_workspaces;
 
+// Stream ids seen by this host thread, by handle: a stream being captured
+// into a graph cannot be asked for its id, so a captured call finds its
+// workspace through the id recorded at this thread's last eager call on the
+// same handle (for the per-thread default stream, this thread's stream).
+thread_local std::unordered_map<uintptr_t, unsigned long long> t_stream_ids;
+
 bwg_status get_workspace(cudaStream_t stream, size_t ws_bytes, int n_counters, Workspace* out) {
   int dev = 0;
-  unsigned long long sid = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaStreamGetId(stream, &sid) != cudaSuccess) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
     cudaGetLastError();
     return BWG_ERR_CUDA;
+  }
+  const bool capturing = cap != cudaStreamCaptureStatusNone;
+  const uintptr_t handle = reinterpret_cast<uintptr_t>(stream);
+  unsigned long long sid = 0;
+  if (!capturing) {
+    if (cudaStreamGetId(stream, &sid) != cudaSuccess) {
+      cudaGetLastError();
+      return BWG_ERR_CUDA;
+    }
+    t_stream_ids[handle] = sid;
+  } else {
+    const auto it = t_stream_ids.find(handle);
+    if (it == t_stream_ids.end()) return BWG_ERR_UNSUPPORTED;  // no eager call on this stream yet
+    sid = it->second;
   }
   std::lock_guard<std::mutex> lock(g_mu);
   Workspace& w = g_workspaces[WorkspaceKey{dev, sid}];
   if (w.ws_bytes < ws_bytes || w.n_counters < n_counters) {
-    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
-      cudaGetLastError();
-      return BWG_ERR_CUDA;
-    }
-    if (cap != cudaStreamCaptureStatusNone) return BWG_ERR_UNSUPPORTED;
+    if (capturing) return BWG_ERR_UNSUPPORTED;
     // grow to cover both the old and the new request, so that alternating
     // shapes settle on one buffer instead of reallocating every call
     const size_t wb = std::max(ws_bytes, w.ws_bytes);

@@ -66,7 +66,7 @@ typedef enum { BWG_OUT_BF16 = 0, BWG_OUT_FP32 = 1, BWG_OUT_FP16 = 2 } bwg_out_dt
  *   default stream of each host thread has its own).  A call that would have
  *   to grow that workspace while its stream is being captured into a CUDA
  *   graph returns BWG_ERR_UNSUPPORTED: make one eager call of the largest
- *   shape on the stream first.  Callers that must never see the library
+ *   shape on the stream first, from the host thread that captures.  Callers that must never see the library
  *   allocate can use gemm_bf16_small_m_noalloc below.
  *   The library also holds a TMA-multicast variant of the pair kernel (two
  *   CTA pairs receive every box of B), selected only by the environment

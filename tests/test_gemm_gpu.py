@@ -398,6 +398,91 @@ def test_small_m_streamk_on_a_side_stream():
     assert np.array_equal(D.cpu().double().numpy(), Dref)
 
 
+def test_small_m_streamk_per_thread_default_streams(monkeypatch):
+    """Two host threads run stream-K small-M products at once on their
+    per-thread default streams: one handle (cudaStreamPerThread), two
+    streams.  Each stream has its own partial-sum workspace, so both results
+    are exact, every time."""
+    import threading
+    from blackwell_tensor_core_gb300 import ops
+    monkeypatch.setenv("BWG_STREAMK", "1")
+    per_thread = 2  # cudaStreamPerThread
+    g = wl.generator(5750)
+    cases = []
+    for i in range(2):
+        A = wl.randint_matrix(72, 4096, -2, 2, g)
+        B = wl.randint_matrix(4096, 3000 + 128 * i, -2, 2, g)
+        Dref, _ = oracle.gemm(wl.bits(A), wl.bits(B))
+        cases.append((A.cuda(), B.cuda(), Dref))
+    assert ops.plan(72, 3000, 4096).streamk == 1
+    results = [[], []]
+    errors = []
+    dev = torch.cuda.current_device()
+
+    def run(i):
+        try:
+            torch.cuda.set_device(dev)
+            Ad, Bd, _ = cases[i]
+            M, K = Ad.shape
+            N = Bd.shape[1]
+            Ds = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in range(20)]
+            torch.cuda.synchronize()
+            for D in Ds:
+                ops.gemm_bf16(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K, K, N, N, wl.OUT_FP32,
+                              per_thread)
+                results[i].append(D)
+            torch.cuda.synchronize()
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    assert ops.last_device_error()[0] == 0
+    for i in range(2):
+        for D in results[i]:
+            assert np.array_equal(D.cpu().double().numpy(), cases[i][2])
+
+
+def test_small_m_streamk_workspace_growth_refused_during_capture(monkeypatch):
+    """A stream-K call that would have to grow its stream's workspace while
+    the stream is being captured returns BWG_ERR_UNSUPPORTED, enqueues
+    nothing and leaves the capture valid; after an eager call of that shape
+    on the stream the same call records, and the replay is exact."""
+    from blackwell_tensor_core_gb300 import ops
+    monkeypatch.setenv("BWG_STREAMK", "1")
+    g = wl.generator(5760)
+    A = wl.randint_matrix(72, 4096, -2, 2, g).cuda()
+    B = wl.randint_matrix(4096, 6000, -2, 2, g).cuda()
+    D = torch.zeros((72, 6000), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    L = ops.lib()
+    args = (A.data_ptr(), B.data_ptr(), D.data_ptr(), 72, 6000, 4096, 4096, 6000, 6000, wl.OUT_FP32)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        st = L.gemm_bf16(*args, s.cuda_stream)
+        # a no-op kernel keeps the captured graph non-empty
+        D.add_(0)
+    assert st == 3
+    torch.cuda.synchronize()
+    # eager call on the same stream makes the workspace; capture now records it
+    assert L.gemm_bf16(*args, s.cuda_stream) == 0
+    s.synchronize()
+    graph2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph2, stream=s):
+        assert L.gemm_bf16(*args, s.cuda_stream) == 0
+    D.zero_()
+    graph2.replay()
+    torch.cuda.synchronize()
+    Dref, _ = oracle.gemm(wl.bits(A.cpu()), wl.bits(B.cpu()))
+    assert np.array_equal(D.cpu().double().numpy(), Dref)
+
+
 @pytest.mark.parametrize("tile_n", [64, 80, 112, 128])
 @pytest.mark.parametrize("out", [wl.OUT_BF16, wl.OUT_FP32])
 @pytest.mark.parametrize("N", [1000, 1024])
