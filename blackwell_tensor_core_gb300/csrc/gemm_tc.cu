@@ -653,7 +653,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
           if (c0 + 32 >= npad) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
+            if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader0 + 8u * acc);
           }
           if (col < p.N) {
 #pragma unroll
@@ -690,7 +690,7 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
       auto release_acc = [&]() {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
+        if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader0 + 8u * acc);
         if (tracer) trec[4] = globaltimer_ns();
       };
       // Stream-K segment of a tile shared by several pairs: every sharer

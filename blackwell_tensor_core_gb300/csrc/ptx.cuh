@@ -97,6 +97,18 @@ BWG_DEV void mbar_arrive_cluster(uint32_t cluster_bar) {
                : "memory");
 }
 
+// The same arrive without release ordering, for handing a TMEM accumulator
+// back to the MMA warp: the arriving warp's tcgen05.ld reads have completed
+// before it arrives (tcgen05.wait::ld blocks until they have), so nothing
+// the warp did before needs ordering against the MMAs the arrive unblocks.
+// A release at cluster scope would wait for every earlier store of the warp
+// (spilled registers, output staging) to be performed: 1100-1800 SM clocks
+// per hand-back on GB300, against 25-50 for this form.
+BWG_DEV void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+
 // Address of the same shared-memory offset in CTA `rank` of this cluster.
 BWG_DEV uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t out;
