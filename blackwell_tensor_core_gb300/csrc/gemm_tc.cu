@@ -381,7 +381,10 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
       const bool ok = clc_query(clc_resp(s), &x);
       if (ok && arm) mbar_arrive_expect_tx(clc_full(s), 16);
       if (warp_wide) __syncwarp();
-      if (!warp_wide || lane == 0) mbar_arrive_cluster(mapa_shared(clc_empty(s), leader));
+      // relaxed: the response was read into registers (the query consumed
+      // the load) before the arrive issues, which is all the slot's next
+      // asynchronous write must wait for
+      if (!warp_wide || lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(clc_empty(s), leader));
       ++k;
       return ok ? static_cast<int>(x) / CG : -1;
     }

@@ -97,13 +97,15 @@ BWG_DEV void mbar_arrive_cluster(uint32_t cluster_bar) {
                : "memory");
 }
 
-// The same arrive without release ordering, for handing a TMEM accumulator
-// back to the MMA warp: the arriving warp's tcgen05.ld reads have completed
-// before it arrives (tcgen05.wait::ld blocks until they have), so nothing
-// the warp did before needs ordering against the MMAs the arrive unblocks.
-// A release at cluster scope would wait for every earlier store of the warp
-// (spilled registers, output staging) to be performed: 1100-1800 SM clocks
-// per hand-back on GB300, against 25-50 for this form.
+// The same arrive without release ordering.  For arrivals that hand back a
+// resource whose last use by the arriving warp has already completed in
+// registers: a TMEM accumulator after tcgen05.wait::ld (which blocks until the
+// reads are done), a response slot after the query that consumed its load.
+// Nothing the warp did before needs ordering against what the arrive
+// unblocks, and a release at cluster scope would wait for every earlier
+// memory operation of the warp to be performed (spilled registers, output
+// staging, and for the MMA warp its MMAs in flight): 1100-5000 SM clocks per
+// arrive measured on GB300, against 25-50 for this form.
 BWG_DEV void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
