@@ -310,6 +310,34 @@ def test_grouped_schedule_covers_every_row_and_column_once(ops):
     assert (covered == 1).all()
 
 
+def test_grouped_tile_group_lookup_matches_a_scan(ops):
+    # The device finds a unit's group by bisection over the prefix of tiles
+    # per group; it must agree with a plain scan, also with runs of empty
+    # groups at the start, in the middle and at the end.
+    rng = np.random.default_rng(11)
+    N, tile_m = 512, 512
+    n_tiles = 2
+    for trial in range(40):
+        G = int(rng.integers(1, 65))
+        counts = rng.integers(0, 1500, size=G)
+        counts[rng.random(G) < 0.3] = 0
+        offsets = [0] + [int(x) for x in np.cumsum(counts)]
+        ok, prefix, lo, hi = _schedule(ops, offsets, N, tile_m)
+        assert ok == 1
+        P = (ctypes.c_int * (G + 1))(*prefix)
+        L = (ctypes.c_int * G)(*lo)
+        H = (ctypes.c_int * G)(*hi)
+        g, m0, n0, re_ = (ctypes.c_int() for _ in range(4))
+        for t in range(prefix[-1]):
+            ops.lib().bwg_grouped_tile(t, G, P, L, H, tile_m, ctypes.byref(g), ctypes.byref(m0),
+                                       ctypes.byref(n0), ctypes.byref(re_))
+            want = 0
+            while want + 1 < G and prefix[want + 1] <= t:
+                want += 1
+            assert g.value == want, (trial, t)
+            assert counts[want] > 0
+
+
 def test_grouped_schedule_flags_bad_offsets(ops):
     assert _schedule(ops, [0, 10, 5, 20], 256, 256)[0] == 0      # decreasing
     assert _schedule(ops, [3, 10, 20], 256, 256)[0] == 0         # first != 0
