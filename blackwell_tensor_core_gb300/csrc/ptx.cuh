@@ -102,10 +102,10 @@ BWG_DEV void mbar_arrive_cluster(uint32_t cluster_bar) {
 // registers: a TMEM accumulator after tcgen05.wait::ld (which blocks until the
 // reads are done), a response slot after the query that consumed its load.
 // Nothing the warp did before needs ordering against what the arrive
-// unblocks, and a release at cluster scope would wait for every earlier
-// memory operation of the warp to be performed (spilled registers, output
-// staging, and for the MMA warp its MMAs in flight): 1100-5000 SM clocks per
-// arrive measured on GB300, against 25-50 for this form.
+// unblocks, and a release at cluster scope waits for every earlier memory
+// operation of the warp to be performed: measured on GB300, 1100-1800 SM
+// clocks for an epilogue warp (spilled registers, output staging) and
+// 2000-5600 for the MMA warp at a unit change, against 25-50 for this form.
 BWG_DEV void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
