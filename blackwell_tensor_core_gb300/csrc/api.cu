@@ -1315,6 +1315,18 @@ bwg_status bwg_probe_tma_swizzle(const void* src, void* out, void* stream) {
                                                 static_cast<cudaStream_t>(stream)));
 }
 
+bwg_status bwg_probe_grouped_tables(const int* offsets, int g0, int G, int G_total, int M,
+                                    int num_n_tiles, int tile_m, int* out, void* stream) {
+  if (offsets == nullptr || out == nullptr || G < 1 || G > kMaxGroupsPerLaunch || g0 < 0 ||
+      G_total < g0 + G || M < 0 || num_n_tiles < 1 || tile_m < 1)
+    return BWG_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  bwg_status s = ensure_device(&st);
+  if (s != BWG_OK) return s;
+  return launch_status(launch_probe_grouped_tables(offsets, g0, G, G_total, M, num_n_tiles, tile_m, out,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
 bwg_status bwg_probe_mma(const void* A, const void* B, float* D, int k_steps, int fp16,
                          void* stream) {
   if (A == nullptr || B == nullptr || D == nullptr || k_steps < 1 || k_steps > 4)

@@ -327,10 +327,10 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
   int* t_lo = tab + kMaxGroupsPerLaunch + 1;
   int* t_hi = t_lo + kMaxGroupsPerLaunch;
   if constexpr (GROUPED) {
-    if (threadIdx.x == 64) {
-      const bool ok = grouped_tables(p.group_offsets, p.g_begin, p.G, p.G_total, p.M,
-                                     p.num_n_tiles, kRowsPerCta * CG * NC, t_prefix, t_lo, t_hi);
-      if (!ok && crank == 0) record_fault(p.err, kFaultBadOffsets, 0, 0, 0, 0);
+    if (warp == 2) {  // a warp with no set-up duty
+      const bool ok = grouped_tables_warp(p.group_offsets, p.g_begin, p.G, p.G_total, p.M,
+                                          p.num_n_tiles, kRowsPerCta * CG * NC, t_prefix, t_lo, t_hi);
+      if (!ok && crank == 0 && lane == 0) record_fault(p.err, kFaultBadOffsets, 0, 0, 0, 0);
     }
   }
   if (warp == 0 && lane == 0) {

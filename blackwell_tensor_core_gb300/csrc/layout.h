@@ -224,6 +224,66 @@ BWG_HD bool grouped_tables(const int* offsets, int g0, int G, int G_total, int M
   return ok;
 }
 
+#if defined(__CUDACC__)
+// The same tables built by the 32 lanes of one warp (G <= 64), for the
+// kernels: each lane loads the offsets of groups lane and lane + 32 and the
+// lanes combine them with shuffles, instead of one thread walking the groups
+// one global load after the other.  Step by step the loop above computes
+//   hi[g] = min(M, max(b_g, a_g, hi[g-1])), hi[-1] = 0,
+//   lo[g] = min(M, max(a_g, hi[g-1])),
+// with a_g, b_g the offsets at g and g+1; so hi[g] is min(M, max(0, the
+// running maximum of max(a_j, b_j) over j <= g)), a prefix maximum, and the
+// tile counts' prefix a prefix sum.  Every lane returns the same flag.
+__device__ __forceinline__ bool grouped_tables_warp(const int* offsets, int g0, int G, int G_total,
+                                                     int M, int num_n_tiles, int tile_m, int* prefix,
+                                                     int* lo, int* hi) {
+  const unsigned full = 0xffffffffu;
+  const int lane = static_cast<int>(threadIdx.x & 31u);
+  bool bad = false;
+  int run_max = 0;  // running maximum over the groups of earlier halves
+  int prev_hi = 0;  // hi of the group before this half's first group
+  int carry = 0;    // tiles of the groups of earlier halves
+  for (int h = 0; h < 2 && h * 32 < G; ++h) {
+    const int g = h * 32 + lane;
+    const bool in = g < G;
+    const int a = in ? offsets[g0 + g] : 0;
+    const int b = in ? offsets[g0 + g + 1] : 0;
+    int m = in ? (a > b ? a : b) : run_max;  // inclusive prefix maximum of max(a, b)
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(full, m, d);
+      if (lane >= d && y > m) m = y;
+    }
+    if (run_max > m) m = run_max;
+    const int hi_g = m < M ? m : M;  // m >= run_max >= 0
+    int before = __shfl_up_sync(full, hi_g, 1);
+    if (lane == 0) before = prev_hi;
+    int lo_g = a > before ? a : before;
+    lo_g = lo_g < M ? lo_g : M;
+    if (in) {
+      if (g0 + g == 0 && a != 0) bad = true;
+      if (b < a || a < before || a < 0 || b > M) bad = true;
+    }
+    const int t = in ? ((hi_g - lo_g + tile_m - 1) / tile_m) * num_n_tiles : 0;
+    int incl = t;  // inclusive prefix sum of the tile counts
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(full, incl, d);
+      if (lane >= d) incl += y;
+    }
+    if (in) {
+      prefix[g] = carry + incl - t;
+      lo[g] = lo_g;
+      hi[g] = hi_g;
+    }
+    carry += __shfl_sync(full, incl, 31);
+    run_max = __shfl_sync(full, m, 31);
+    prev_hi = __shfl_sync(full, hi_g, 31);
+  }
+  if (lane == 0) prefix[G] = carry;
+  if (g0 + G == G_total && offsets[G_total] != M) bad = true;
+  return !__any_sync(full, bad);
+}
+#endif
+
 // Tile t of the grouped schedule: its group, first row, first column and the
 // group's row end.  Inside a group the row tile runs fastest, so the few
 // concurrently running tiles of one column strip share that strip of B_g.

@@ -152,6 +152,8 @@ cudaError_t launch_probe_cluster_pair(const float* in, float* sum_out, int* peer
                                       cudaStream_t s);
 cudaError_t launch_probe_tma_swizzle(const CUtensorMap& map, void* out, unsigned long long* err,
                                      unsigned long long timeout_ns, cudaStream_t s);
+cudaError_t launch_probe_grouped_tables(const int* offsets, int g0, int G, int G_total, int M,
+                                        int num_n_tiles, int tile_m, int* out, cudaStream_t s);
 cudaError_t launch_probe_mma(const CUtensorMap& map_a, const CUtensorMap& map_b, float* d, int k_steps,
                              uint32_t idesc, unsigned long long* err, unsigned long long timeout_ns,
                              cudaStream_t s);

@@ -12,6 +12,8 @@
 //  - one tile of tcgen05.mma (M = 128, N = 256, K = 16 per instruction, 1..4
 //    instructions) from TMA-loaded operands with the library's descriptors,
 //    TMEM allocation and tcgen05.ld read-back, compared with an exact product.
+//  - the grouped kernels' warp-parallel schedule tables (grouped_tables_warp),
+//    compared with the one-thread loop that defines them.
 // They are test hooks: nothing on the GEMM path calls them.  Every wait is
 // bounded and reports through the device error word.
 #include "layout.h"
@@ -156,6 +158,23 @@ cudaError_t launch_probe_tma_swizzle(const CUtensorMap& map, void* out, unsigned
                                      unsigned long long timeout_ns, cudaStream_t s) {
   const int smem = 8192 + 1024;
   probe_tma_swizzle_kernel<<<1, 128, smem, s>>>(map, static_cast<uint8_t*>(out), err, timeout_ns);
+  return cudaGetLastError();
+}
+
+namespace {
+// out: prefix[G+1], lo[G], hi[G], ok: 3G + 2 ints.
+__global__ void __launch_bounds__(32) probe_grouped_tables_kernel(const int* offsets, int g0, int G,
+                                                                 int G_total, int M, int num_n_tiles,
+                                                                 int tile_m, int* out) {
+  const bool ok = grouped_tables_warp(offsets, g0, G, G_total, M, num_n_tiles, tile_m, out,
+                                      out + G + 1, out + 2 * G + 1);
+  if (threadIdx.x == 0) out[3 * G + 1] = ok ? 1 : 0;
+}
+}  // namespace
+
+cudaError_t launch_probe_grouped_tables(const int* offsets, int g0, int G, int G_total, int M,
+                                        int num_n_tiles, int tile_m, int* out, cudaStream_t s) {
+  probe_grouped_tables_kernel<<<1, 32, 0, s>>>(offsets, g0, G, G_total, M, num_n_tiles, tile_m, out);
   return cudaGetLastError();
 }
 

@@ -78,7 +78,8 @@ def lib() -> ctypes.CDLL:
             L.bwg_last_device_error.restype = i
             for name, args in (("bwg_probe_cluster_pair", [vp, vp, vp, i, vp]),
                                ("bwg_probe_tma_swizzle", [vp, vp, vp]),
-                               ("bwg_probe_mma", [vp, vp, vp, i, i, vp])):
+                               ("bwg_probe_mma", [vp, vp, vp, i, i, vp]),
+                               ("bwg_probe_grouped_tables", [vp, i, i, i, i, i, i, vp, vp])):
                 f = getattr(L, name)
                 f.argtypes = args
                 f.restype = i

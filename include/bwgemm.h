@@ -255,12 +255,20 @@ void bwg_set_watchdog_ns(unsigned long long ns);
  *   k = k_steps (1..4) tcgen05.mma instructions of K = 16, with A [128, 64]
  *   and B [64, 256] row-major BF16 (fp16 = 0) or FP16 (fp16 = 1), loaded by
  *   TMA and read back from TMEM, with the GEMM kernels' descriptors.
+ * bwg_probe_grouped_tables: the schedule tables of groups g0 .. g0+G-1
+ *   (1 <= G <= 64) that the grouped kernels build from the device int32
+ *   offsets [G_total + 1] with one warp; `out` (device int32, 3G + 2) gets
+ *   the tile prefix [G + 1], the clamped row starts [G] and ends [G], and 1
+ *   or 0 for whether the offsets honour the contract.  The tables equal those
+ *   of the grouped_gemm_* contract's sequential definition.
  */
 bwg_status bwg_probe_cluster_pair(const float* in, float* sum_out, int* peer_out, int n,
                                   void* stream);
 bwg_status bwg_probe_tma_swizzle(const void* src, void* out, void* stream);
 bwg_status bwg_probe_mma(const void* A, const void* B, float* D, int k_steps, int fp16,
                          void* stream);
+bwg_status bwg_probe_grouped_tables(const int* offsets, int g0, int G, int G_total, int M,
+                                    int num_n_tiles, int tile_m, int* out, void* stream);
 
 /*
  * Test hook: adds `bytes` to the transaction count every stage expects, so

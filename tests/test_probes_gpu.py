@@ -88,3 +88,64 @@ def test_single_tile_mma_exact(k_steps, dtype):
     K = 16 * k_steps
     Dref, _ = oracle.gemm(wl.bits(A[:, :K].contiguous()), wl.bits(B[:K].contiguous()), dtype)
     assert np.array_equal(D.cpu().double().numpy(), Dref)
+
+
+def _tables_by_loop(offsets, g0, G, G_total, M, n_tiles, tile_m):
+    """The grouped schedule tables by their sequential definition: one group
+    after the other, each row range clamped into [0, M] and after the previous
+    group's end."""
+    ok, tiles, prev_hi = True, 0, 0
+    prefix, lo, hi = [], [], []
+    for g in range(G):
+        a, b = offsets[g0 + g], offsets[g0 + g + 1]
+        if g0 + g == 0 and a != 0:
+            ok = False
+        if b < a or a < prev_hi or a < 0 or b > M:
+            ok = False
+        a = max(a, prev_hi)
+        a = M if a > M else max(a, 0)
+        b = a if b < a else min(b, M)
+        prev_hi = b
+        prefix.append(tiles)
+        lo.append(a)
+        hi.append(b)
+        tiles += ((b - a + tile_m - 1) // tile_m) * n_tiles
+    prefix.append(tiles)
+    if g0 + G == G_total and offsets[G_total] != M:
+        ok = False
+    return prefix, lo, hi, ok
+
+
+def test_grouped_tables_warp_matches_the_sequential_definition():
+    from blackwell_tensor_core_gb300 import ops
+    rng = np.random.default_rng(21)
+    h = torch.cuda.current_stream().cuda_stream
+    cases = []
+    for G in (1, 2, 7, 31, 32, 33, 63, 64):
+        counts = rng.integers(0, 1200, size=G)
+        counts[rng.random(G) < 0.3] = 0
+        off = [0] + [int(x) for x in np.cumsum(counts)]
+        cases.append((off, 0, G, G, off[-1]))                       # valid
+        bad = list(off)
+        bad[G // 2] += 5000                                          # out of order, past M
+        cases.append((bad, 0, G, G, off[-1]))
+        neg = list(off)
+        neg[0] = -3                                                  # first offset not 0
+        cases.append((neg, 0, G, G, off[-1]))
+        cases.append((off, 0, G, G, off[-1] + 17))                   # last != M
+    long = [0] + [int(x) for x in np.cumsum(rng.integers(0, 900, size=70))]
+    cases.append((long, 0, 64, 70, long[-1]))                        # first launch of 70 groups
+    cases.append((long, 64, 6, 70, long[-1]))                        # second launch
+    cases.append((long, 30, 40, 70, long[-1]))
+    for off, g0, G, G_total, M in cases:
+        for n_tiles, tile_m in ((16, 512), (3, 256)):
+            d_off = torch.tensor(off, dtype=torch.int32, device="cuda")
+            out = torch.full((3 * G + 2,), -7, dtype=torch.int32, device="cuda")
+            _check(ops.lib().bwg_probe_grouped_tables(d_off.data_ptr(), g0, G, G_total, M, n_tiles, tile_m,
+                                                      out.data_ptr(), h))
+            got = out.cpu().tolist()
+            prefix, lo, hi, ok = _tables_by_loop(off, g0, G, G_total, M, n_tiles, tile_m)
+            assert got[:G + 1] == prefix, (g0, G, M)
+            assert got[G + 1:2 * G + 1] == lo, (g0, G, M)
+            assert got[2 * G + 1:3 * G + 1] == hi, (g0, G, M)
+            assert got[3 * G + 1] == (1 if ok else 0), (g0, G, M)
