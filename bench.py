@@ -378,16 +378,17 @@ def cublas_context(ops, stream, dev, reps=40):
             "launches_each": n}
 
 
-def alternate_with_cublas(ops, ours, theirs, stream, reps):
+def alternate_with_cublas(ops, ours, theirs, stream, reps, between=None):
     """Medians (ms) of CUDA-event times of `ours` and `theirs`, launched
-    alternately in blocks of 10 after three untimed launches of each."""
+    alternately in blocks of 10 after three untimed launches of each;
+    `between` (e.g. an L2 flush) runs before every timed launch of both."""
     for _ in range(3):
         ours()
         theirs()
     to, tc = [], []
     for _ in range(reps // 10):
-        to += time_launches(ours, 10, stream, keep_ahead=True)[1]
-        tc += time_launches(theirs, 10, stream, keep_ahead=True)[1]
+        to += time_launches(ours, 10, stream, between=between, keep_ahead=True)[1]
+        tc += time_launches(theirs, 10, stream, between=between, keep_ahead=True)[1]
     check_device_error(ops)
     return statistics.median(to), statistics.median(tc), len(to)
 
@@ -439,6 +440,13 @@ def _variant_square(ops, wl, stream, peaks, steps, warm, dev):
                           "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
                                        "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"]},
                           "l2": "flushed (256 MiB write) before every timed launch"}
+    # context: torch.matmul (cuBLAS) on the same inputs, alternated, the
+    # same flush before every timed launch of either
+    D2 = torch.empty_like(D)
+    mo, mc, n = alternate_with_cublas(ops, launch, lambda i=0: torch.matmul(A, B, out=D2), stream, 40,
+                                      between=lambda i: flush.zero_())
+    out["square_4096"]["context_cublas"] = {"ours_ms_median": mo, "cublas_ms_median": mc,
+                                            "ours_over_cublas": mc / mo, "launches_each": n}
     return out
 
 
