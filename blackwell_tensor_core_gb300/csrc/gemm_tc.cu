@@ -390,6 +390,16 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
     }
   };
 
+  if constexpr (NC == 2) {
+    // Registers move from warpgroup 0 (TMA and MMA issue: loop state and
+    // descriptors) to the epilogue warpgroups, which hold a whole 32 x 256
+    // accumulator slice (packed to 16 bits) before the hand-back.
+    if (warp < 4)
+      setmaxnreg_dec<kRegsControl2C>();
+    else
+      setmaxnreg_inc<kRegsEpilogue2C>();
+  }
+
   if (warp == 0) {
     // ---- TMA producer: one thread streams A and B k-blocks into the ring ----
     if (lane == 0) {
@@ -806,21 +816,27 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
       if constexpr (NC == 2) {
         if (early) {
           if constexpr (SW) {
+            // one TMEM round trip per 64 output columns: gate and up, 128
+            // registers in flight
             uint32_t pks[2][32];
 #pragma unroll
             for (int sub = 0; sub < 2; ++sub) {
               if (sub < nsub) {
+                uint32_t g[2][32], u[2][32];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                  uint32_t g[32], u[32];
-                  tmem_ld_32x32b_x32(t_acc + sub * 64 + h * 32, g);
-                  tmem_ld_32x32b_x32(t_acc + out_cols + sub * 64 + h * 32, u);
-                  tmem_wait_ld();
+                  tmem_ld_32x32b_x32(t_acc + sub * 64 + h * 32, g[h]);
+                  tmem_ld_32x32b_x32(t_acc + out_cols + sub * 64 + h * 32, u[h]);
+                }
+                tmem_wait_ld();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
 #pragma unroll
                   for (int i = 0; i < 16; ++i) {
-                    const float y0 = swiglu_f32(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]));
-                    const float y1 =
-                        swiglu_f32(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]));
+                    const float y0 =
+                        swiglu_f32(__uint_as_float(g[h][2 * i]), __uint_as_float(u[h][2 * i]));
+                    const float y1 = swiglu_f32(__uint_as_float(g[h][2 * i + 1]),
+                                                __uint_as_float(u[h][2 * i + 1]));
                     pks[sub][16 * h + i] = outbf ? pack_bf16x2(y0, y1) : pack_f16x2(y0, y1);
                   }
                 }
@@ -832,32 +848,36 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
               if (sub < nsub) emit(sub, pks[sub]);
           } else {
             // All four 64-column sub-tiles are read and packed (128
-            // registers, a few values spill) before the hand-back; staging
-            // sub-tile 0 first and holding three measured 0.7 us longer per
-            // tile, as its stores slowed the remaining TMEM reads.
-            auto load_packed = [&](int sub, uint32_t (&pk)[32]) {
+            // registers) before the hand-back, two sub-tiles (128 FP32
+            // registers in flight) per TMEM round trip; staging sub-tile 0
+            // first and holding three measured 0.7 us longer per tile, as its
+            // stores slowed the remaining TMEM reads.  Columns past the
+            // unit's width are read (they are inside the accumulator) and
+            // not stored.
+            auto pack = [&](uint32_t lo, uint32_t hi) {
+              return outbf ? pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi))
+                           : pack_f16x2(__uint_as_float(lo), __uint_as_float(hi));
+            };
+            auto load_packed2 = [&](int sub, uint32_t (&pa)[32], uint32_t (&pb)[32]) {
+              uint32_t v[4][32];
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(t_acc + sub * 64 + h * 32, v);
-                tmem_wait_ld();
+              for (int h = 0; h < 4; ++h) tmem_ld_32x32b_x32(t_acc + sub * 64 + h * 32, v[h]);
+              tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  const float lo = __uint_as_float(v[2 * i]), hi = __uint_as_float(v[2 * i + 1]);
-                  pk[16 * h + i] = outbf ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
-                }
+              for (int i = 0; i < 16; ++i) {
+                pa[i] = pack(v[0][2 * i], v[0][2 * i + 1]);
+                pa[16 + i] = pack(v[1][2 * i], v[1][2 * i + 1]);
+                pb[i] = pack(v[2][2 * i], v[2][2 * i + 1]);
+                pb[16 + i] = pack(v[3][2 * i], v[3][2 * i + 1]);
               }
             };
-            uint32_t pk0[32], pka[3][32];
-            load_packed(0, pk0);
-#pragma unroll
-            for (int sub = 1; sub < 4; ++sub)
-              if (sub < nsub) load_packed(sub, pka[sub - 1]);
+            uint32_t pk[4][32];
+            load_packed2(0, pk[0], pk[1]);
+            load_packed2(2, pk[2], pk[3]);
             release_acc();
-            emit(0, pk0);
 #pragma unroll
-            for (int sub = 1; sub < 4; ++sub)
-              if (sub < nsub) emit(sub, pka[sub - 1]);
+            for (int sub = 0; sub < 4; ++sub)
+              if (sub < nsub) emit(sub, pk[sub]);
           }
         }
       }
@@ -1012,6 +1032,28 @@ cudaError_t launch_cluster(K kernel, const P& p, int cg, int grid, size_t smem, 
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+// The two-consumer kernels split their registers with setmaxnreg after
+// set-up; the epilogue warpgroups' increase only completes if the CTA was
+// launched with at least the registers the split hands out.  Checked once
+// per kernel from the compiled register count: a smaller allocation would
+// leave the increase waiting for registers that never come free, so such a
+// kernel is not launched.
+template <class K>
+bool two_consumer_regs_ok(K kernel) {
+  static const bool ok = [kernel] {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, kernel) != cudaSuccess) return false;
+    return static_cast<uint32_t>(a.numRegs) * kThreads2C >= kRegsControl2C * 128u + kRegsEpilogue2C * 256u;
+  }();
+  return ok;
+}
+
+template <class K, class P>
+cudaError_t launch_two_consumer(K kernel, const P& p, int grid, size_t smem, cudaStream_t s) {
+  if (!two_consumer_regs_ok(kernel)) return cudaErrorLaunchOutOfResources;
+  return launch_cluster(kernel, p, 2, grid, smem, s, kThreads2C);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_1cta(const GemmParams& p, int grid, size_t smem, cudaStream_t s) {
@@ -1028,19 +1070,17 @@ cudaError_t launch_gemm_2cta_mc(const GemmParams& p, int grid, size_t smem, cuda
 
 cudaError_t launch_gemm_2cta_2c(const GemmParams& p, int grid, size_t smem, cudaStream_t s,
                                 bool dynamic) {
-  return dynamic ? launch_cluster(gemm_dense_2c_kernel<true>, p, 2, grid, smem, s, kThreads2C)
-                 : launch_cluster(gemm_dense_2c_kernel<false>, p, 2, grid, smem, s, kThreads2C);
+  return dynamic ? launch_two_consumer(gemm_dense_2c_kernel<true>, p, grid, smem, s)
+                 : launch_two_consumer(gemm_dense_2c_kernel<false>, p, grid, smem, s);
 }
 
 cudaError_t launch_grouped_2c(const GroupedParams& p, int grid, size_t smem, cudaStream_t s,
                               bool swiglu, bool dynamic) {
   if (dynamic)
-    return swiglu
-               ? launch_cluster(gemm_grouped_2c_kernel<true, true>, p, 2, grid, smem, s, kThreads2C)
-               : launch_cluster(gemm_grouped_2c_kernel<false, true>, p, 2, grid, smem, s, kThreads2C);
-  return swiglu
-             ? launch_cluster(gemm_grouped_2c_kernel<true, false>, p, 2, grid, smem, s, kThreads2C)
-             : launch_cluster(gemm_grouped_2c_kernel<false, false>, p, 2, grid, smem, s, kThreads2C);
+    return swiglu ? launch_two_consumer(gemm_grouped_2c_kernel<true, true>, p, grid, smem, s)
+                  : launch_two_consumer(gemm_grouped_2c_kernel<false, true>, p, grid, smem, s);
+  return swiglu ? launch_two_consumer(gemm_grouped_2c_kernel<true, false>, p, grid, smem, s)
+                : launch_two_consumer(gemm_grouped_2c_kernel<false, false>, p, grid, smem, s);
 }
 
 cudaError_t launch_grouped_2cta(const GroupedParams& p, int grid, size_t smem, cudaStream_t s,

@@ -10,6 +10,15 @@ namespace bwg {
 
 constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kThreads2C = 384;      // two-consumer pair kernel: 12 warps
+// Registers per thread of the two-consumer kernel: at launch (one CTA per SM,
+// 65,536 / 384 rounded down to a multiple of 8), and the split after set-up
+// between warpgroup 0 (TMA, MMA) and the two epilogue warpgroups.
+constexpr uint32_t kRegsLaunch2C = 168;
+constexpr uint32_t kRegsControl2C = 56;
+constexpr uint32_t kRegsEpilogue2C = 224;
+static_assert(kRegsControl2C * 128 + kRegsEpilogue2C * 256 <= kRegsLaunch2C * kThreads2C,
+              "the register split must fit in the launch allocation");
+static_assert(kRegsLaunch2C * kThreads2C <= 65536, "one CTA per SM");
 constexpr int kBK = 64;              // K per stage: one 128-byte swizzle row of 16-bit data
 constexpr int kTileN = 256;          // output columns per tile (MMA N)
 constexpr int kRowsPerCta = 128;     // accumulator rows per CTA (TMEM lanes)

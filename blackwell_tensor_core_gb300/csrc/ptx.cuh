@@ -474,6 +474,21 @@ BWG_DEV void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
       : "memory");
 }
 
+// Per-warpgroup register budgets (all four warps of a warpgroup execute the
+// same form).  `dec` returns registers to the CTA's pool; `inc` blocks until
+// the pool holds enough, so the budgets of all warpgroups must add up to at
+// most the registers the CTA was launched with.
+template <uint32_t R>
+BWG_DEV void setmaxnreg_dec() {
+  static_assert(R >= 24 && R <= 256 && R % 8 == 0, "register budget");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <uint32_t R>
+BWG_DEV void setmaxnreg_inc() {
+  static_assert(R >= 24 && R <= 256 && R % 8 == 0, "register budget");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+
 BWG_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Warp-collective TMEM load: lane i of the warp reads TMEM lane (base lane + i),
