@@ -194,3 +194,36 @@ def test_grouped_dynamic_schedule(swiglu, monkeypatch):
     else:
         Dref, _ = oracle.grouped_gemm(wl.bits(A), [wl.bits(b) for b in Bs], off)
         assert_bits_equal(out.cpu(), oracle.round_to(Dref, "bf16"), "grouped dynamic")
+
+
+SHORT_END_COUNTS = [31, 512 + 32, 33, 63, 64, 65, 0, 100, 127, 128, 129, 1024 + 1, 512 + 64, 7]
+
+
+@pytest.mark.parametrize("sched,swiglu", [("clc", False), ("static", False), ("clc", True)])
+def test_grouped_short_group_ends(sched, swiglu, monkeypatch):
+    """Two-consumer kernel, group ends of 1..129 rows (31, 32, 33, 63, 64,
+    65, 100, 127, 128, 129 and 1 past a multiple of 512), an empty group, and
+    a last group of 7 rows whose 128-row A boxes reach past the end of A:
+    exact on integer inputs, within the SwiGLU bound with the fused epilogue."""
+    from blackwell_tensor_core_gb300 import ops
+    monkeypatch.setenv("BWG_SCHED", sched)
+    counts = SHORT_END_COUNTS
+    off = wl.offsets_from_counts(counts)
+    g = wl.generator(6700)
+    K, N = 192, 528
+    A = wl.randint_matrix(int(off[-1]), K, -2, 2, g)
+    Bs = [wl.randint_matrix(K, N, -2, 2, g) for _ in counts]
+    dev = torch.device("cuda")
+    offd = torch.from_numpy(off).to(dev)
+    out = torch.full((A.shape[0], N // 2 if swiglu else N), float("nan"), dtype=A.dtype, device=dev)
+    ops.grouped_gemm(A.to(dev), [b.to(dev) for b in Bs], offd, out=out, swiglu=swiglu)
+    torch.cuda.synchronize()
+    st, word = ops.last_device_error()
+    assert st == 0, hex(word)
+    if swiglu:
+        Href, W = oracle.grouped_swiglu(wl.bits(A), [wl.bits(b) for b in Bs], off)
+        bad = oracle.bound_violations(out.cpu().double().numpy(), Href, W)
+        assert not bad.any(), "%d outside the SwiGLU bound" % bad.sum()
+    else:
+        Dref, _ = oracle.grouped_gemm(wl.bits(A), [wl.bits(b) for b in Bs], off)
+        assert_bits_equal(out.cpu(), oracle.round_to(Dref, "bf16"), "short group ends %s" % sched)
