@@ -820,6 +820,27 @@ bwg_status run_dense(bool fp16_in, const void* A, const void* B, void* D, int M,
       !get_map(&p.map_d, D, out_map_dtype(out_dtype), N, M, static_cast<uint64_t>(ldd) * oe,
                d_box_inner, 32, CU_TENSOR_MAP_SWIZZLE_128B))
     return BWG_ERR_CUDA;
+  {
+    // One B load a stage per pair CTA (its two 64-column chunks): [K, N] as
+    // a 3-D view, which needs N a multiple of 64 so that no chunk reaches past
+    // a row; [N, K] as a 128-row box.  BWG_B_ONE_BOX=0 turns it off.
+    const char* v = std::getenv("BWG_B_ONE_BOX");
+    const bool on = !(v != nullptr && v[0] == '0') && (b_kmajor || N % 64 == 0);
+    if (on) {
+      bool ok;
+      if (b_kmajor) {
+        ok = get_map(&p.map_b1, B, in_t, K, N, static_cast<uint64_t>(ldb) * 2, 64, 128,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+      } else {
+        const uint64_t dims[3] = {64, static_cast<uint64_t>(K), static_cast<uint64_t>(N / 64)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(ldb) * 2, 128};
+        const uint32_t box[3] = {64, 64, 2};
+        ok = get_map_nd(&p.map_b1, B, in_t, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+      }
+      if (!ok) return BWG_ERR_CUDA;
+      p.b_one_box = 1;
+    }
+  }
   p.err = st->err;
   p.d_ptr = D;
   p.timeout_ns = g_timeout_ns.load();

@@ -472,9 +472,17 @@ __device__ void gemm_body(const PT& P, const GemmParams& p) {
               if ((tl.cmask >> c) & 1)
                 tma_load_2d_pair(sa + c * kAStageBytes, &p.map_a, fb, k0, a_row + c * 2 * kRowsPerCta);
             if constexpr (MC == 1) {
-              for (uint32_t j = 0; j < b_chunks; ++j) {
-                const int c = b_col + 64 * static_cast<int>(j);
-                tma_load_2d_pair(sb + j * kBChunkBytes, mb, fb, bk ? k0 : c, bk ? c : k0);
+              if (!GROUPED && p.b_one_box && b_chunks == 2) {
+                // both 64-column chunks in one load
+                if (bk)
+                  tma_load_2d_pair(sb, &p.map_b1, fb, k0, b_col);
+                else
+                  tma_load_3d_pair(sb, &p.map_b1, fb, 0, k0, b_col / 64);
+              } else {
+                for (uint32_t j = 0; j < b_chunks; ++j) {
+                  const int c = b_col + 64 * static_cast<int>(j);
+                  tma_load_2d_pair(sb + j * kBChunkBytes, mb, fb, bk ? k0 : c, bk ? c : k0);
+                }
               }
             } else {
               // The pairs share B: box j of this CTA's columns is fetched once, by

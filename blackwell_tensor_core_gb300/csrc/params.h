@@ -47,6 +47,12 @@ struct GemmParams {
   CUtensorMap map_b;  // B [K, N], box {64 (N), 64 (K)}; or B [N, K] (b_kmajor), box {64 (K), 64 (N)};
                       // 128B swizzle (dense only)
   CUtensorMap map_d;  // D [rows, N], box {64 or 32 (N), 32 (rows)}, 128B swizzle
+  // B, one load for a pair CTA's 128 columns of a stage (b_one_box): [K, N]
+  // as a 3-D view {64 (N in a chunk), K, N/64 chunks} with box {64, 64, 2};
+  // [N, K] (b_kmajor) as 2-D with box {64 (K), 128 (N)}.  Either lands exactly
+  // as the two 64-column boxes of map_b would.
+  CUtensorMap map_b1;
+  int b_one_box;      // 1: map_b1 is valid and the pair kernels use it (dense only)
   unsigned long long* err;
   void* d_ptr;               // D base, for masked row stores at ragged group ends
   const int* group_offsets;  // grouped only: device int32 [G+1]

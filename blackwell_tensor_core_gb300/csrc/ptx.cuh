@@ -299,6 +299,15 @@ BWG_DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar
       : "memory");
 }
 
+BWG_DEV void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                              int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 // Pair form with cluster multicast: the box lands at offset `dst` in every
 // CTA of `cta_mask`, and each destination's bytes complete on the barrier at
 // offset `bar` in that destination's pair-leader CTA (`bar` addresses a leader).
