@@ -313,6 +313,9 @@ void bwg_debug_set_trace(void* buffer);
  *   BWG_SMALL_M_PAIRS  0: fill the small-M stage ring one stage per load
  *   BWG_GROUPED_1C     1: grouped kernels with one MMA consumer (256-row units)
  *   BWG_GROUPED_SWAP   1: swapped-operand group ends (one-consumer grouped kernel)
+ *   BWG_B_ONE_BOX      0: dense pair kernels load a CTA's B stage as two
+ *                      64-column boxes (default: one load where N % 64 == 0
+ *                      or B is [N, K])
  * ------------------------------------------------------------------- */
 
 /* ---------------------------------------------------------------------
