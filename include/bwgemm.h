@@ -311,6 +311,8 @@ void bwg_debug_set_trace(void* buffer);
  *   BWG_SMALL_M_SPLIT  0: no cluster split; F (2..8): that cluster size
  *   BWG_STREAMK        1 / 0: force stream-K on / off in the small-M kernel
  *   BWG_SMALL_M_PAIRS  0: fill the small-M stage ring one stage per load
+ *   BWG_SMALL_M_L2HINT small-M L2 policies, bit 1: B^T evict-first, bit 0: A
+ *                      evict-last (default 2; 0 with the cluster split)
  *   BWG_GROUPED_1C     1: grouped kernels with one MMA consumer (256-row units)
  *   BWG_GROUPED_SWAP   1: swapped-operand group ends (one-consumer grouped kernel)
  *   BWG_B_ONE_BOX      0: dense pair kernels load a CTA's B stage as two

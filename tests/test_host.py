@@ -487,3 +487,22 @@ def test_host_buffer_binding_checks_shapes_and_buffers(ops):
         ops.gemm_bf16_host(hA.t().contiguous().t(), hB, hD, *dev)
     with pytest.raises(ValueError, match="dA must be a dense CUDA buffer of at least 4096 bytes"):
         ops.gemm_bf16_host(hA, hB, hD, *dev)
+
+
+def test_every_planner_override_is_documented_in_the_header():
+    """Each BWG_* environment variable the library reads is listed in the
+    public header's planner-override block."""
+    import re
+    csrc = os.path.join(ROOT, "blackwell_tensor_core_gb300", "csrc")
+    read = set()
+    for name in os.listdir(csrc):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                read |= set(re.findall(r'getenv\("(BWG_[A-Z0-9_]+)"\)', f.read()))
+    with open(os.path.join(ROOT, "include", "bwgemm.h"), encoding="utf-8") as f:
+        header = f.read()
+    block = header[header.index("Planner overrides"):]
+    block = block[:block.index("*/")]
+    listed = set(re.findall(r"\*\s+(BWG_[A-Z0-9_]+)\s", block))
+    assert read, "no overrides found"
+    assert read <= listed, "undocumented: %s" % sorted(read - listed)
