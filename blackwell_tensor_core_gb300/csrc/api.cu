@@ -328,9 +328,10 @@ bwg_status plan_dense(int M, int N, int K, int out_dtype, bool fp16_in, int sm_c
   }
   int kind = force_kernel;
   if (kind == 0) {
-    // 512x256 tiles (two MMA consumers per pair) need 25% fewer shared-memory
-    // bytes per FLOP than 256x256 ones, which is what limits these kernels;
-    // use them while they still give every pair at least one tile.
+    // 512x256 tiles (two MMA consumers per pair) do twice the MMA work of
+    // 256x256 ones for each ring stage filled, and the filling of stages, not
+    // the tensor pipe, is what limits the one-consumer tiles; use them while
+    // they still give every pair at least one tile.
     const int pairs = max_clusters_2c > 0 ? max_clusters_2c : sm_count / 2;
     const long long tiles_2c = static_cast<long long>(ceil_div(M, 4 * kRowsPerCta)) * ceil_div(N, kTileN);
     if (M <= kSmallMMaxM)
